@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the Engram layer forward (one GB300 per rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one engram_forward (gather + dequantise -> tcgen05 wkv projection ->
+gate + residual add) over one batch of synthetic inputs resident in HBM.  The
+default workload is the decode batch (B=64, T=1, 24 prime row ranges above
+2^20: 25,169,534 rows, 6.4 GB of fp8 codes), the configuration the layer's
+tokens/s metric is quoted on; the other workloads (tiny, Zipf prefill, skewed
+decode, full-size table) are selectable with --workload and are parity-test
+cases.
+
+One JSON line is printed by rank 0 (see the keys below).  `value` is tokens/s
+over all ranks, timed on the device with CUDA events around each step; the L2
+is flushed (a 256 MB write) between timed steps, outside the events.  `e2e`
+times the same call with the inputs in pinned host memory: the host->device
+copies of hash_ids, x and the mask and the device->host copy of the output are
+inside its timed region.  `roofline` describes the dominant kernel (the wkv
+projection) from its own CUDA-event durations; `cpu_baseline` is the CPU oracle
+timed on a bounded sample of the same workload.  `--impl reference` times the
+oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Engram layer tokens/s (prefill, decode); gather HBM GB/s; % of roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "decode_64x1"
+FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def algorithmic(w, M):
+    """Bytes and FLOPs the layer must move / compute for M tokens: per token
+    the ids (n_cols*8), codes (n_cols*head_dim), scales, x and out (hc*dim*2
+    each) and the mask byte; per call the wkv weight and q/k weights."""
+    nb = w.head_dim // w.scale_block
+    per_tok = (w.n_cols * 8 + w.n_cols * w.head_dim + w.n_cols * nb * 4 + 2 * w.hc_mult * w.dim * 2 + 1)
+    per_call = w.N * w.K * 2 + 2 * w.hc_mult * w.dim * 2
+    flops = 2.0 * w.N * w.K * M
+    return per_tok * M + per_call, flops
+
+
+def projection_bytes(w, M):
+    """Algorithmic bytes of one projection launch: the weight once, the
+    gathered rows read once, kv written once in bf16."""
+    return w.N * w.K * 2 + M * w.K * 2 + M * w.N * 2
+
+
+def gather_bytes(w, M):
+    nb = w.head_dim // w.scale_block
+    return M * (w.n_cols * 8 + w.n_cols * w.head_dim + w.n_cols * nb * 4 + w.K * 2)
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["engram_hashed_gram_gb300/csrc/gemm.cu", "engram_hashed_gram_gb300/csrc/common.cuh",
+                "engram_hashed_gram_gb300/csrc/internal.cuh"]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the projection kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "wkv_gemm_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    digest = source_digest(GEMM_SOURCES)
+    for line in open(p):
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if kv.get("workload") == workload and kv.get("source_sha256") == digest:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.marks = []
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 1.3 * min(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(busy)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_oracle_run(w, inp, min_seconds=12.0, max_passes=50, tok=None):
+    """Times the oracle as it stands on passes over a bounded token sample;
+    returns (tokens/s, seconds, tokens, description).  Regenerating the table
+    rows the sample references is input generation and is not timed."""
+    import numpy as np
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import engram_oracle as O
+    from parity import compact_rows
+    M = w.M
+    if tok is None:
+        tok = np.arange(min(M, 64))
+    ids = inp.hash_ids.reshape(M, w.n_cols)[tok]
+    cids, codes, scales = compact_rows(w, ids)
+    x = inp.x.reshape(M, w.hc_mult, w.dim)[tok]
+    mask = None if inp.mask is None else inp.mask.reshape(M)[tok]
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        O.forward(cids, x, codes, scales, inp.wkv, inp.q, inp.k, mask, scale_block=w.scale_block, eps=w.eps)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= max_passes:
+            break
+    n = passes * len(tok)
+    desc = f"{passes} pass(es) of the oracle over {len(tok)} of the workload's {M} tokens"
+    return n / el, el, n, desc
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((d.get("num_threads", 0) for d in threadpool_info()), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, w):
+    """The oracle as the reference arm, on the host cores."""
+    from engram_hashed_gram_gb300 import synth
+    import numpy as np
+    inp = synth.make_inputs(w)
+    tok = np.arange(min(w.M, 64))
+    for _ in range(args.warmup):
+        cpu_oracle_run(w, inp, min_seconds=0.0, max_passes=1, tok=tok)
+    times = []
+    for _ in range(args.steps):
+        v, el, n, desc = cpu_oracle_run(w, inp, min_seconds=0.0, max_passes=1, tok=tok)
+        times.append(el)
+    total = sum(times)
+    value = len(tok) * args.steps / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"each step: one oracle pass over {len(tok)} of the workload's {w.M} tokens"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "T": w.T, "tokens": w.M, "dim": w.dim, "hc_mult": w.hc_mult,
+            "n_cols": w.n_cols, "head_dim": w.head_dim, "table_rows": w.num_rows(),
+            "table_gb": round(w.num_rows() * w.head_dim / 1e9, 2), "hash_ids": w.ids, "mask": w.mask,
+            "wkv": "bf16 [25600, 6144]", "l2": "flushed between timed steps (256 MB write)"}
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from engram_hashed_gram_gb300 import build as B
+    from engram_hashed_gram_gb300 import synth
+    from engram_hashed_gram_gb300 import synth_device as SD
+    from engram_hashed_gram_gb300.layer import EngramLayer
+
+    B.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    M = w.M
+    inp = synth.make_inputs(w)
+    table, scale = SD.make_table(w, device=dev)
+    d = SD.upload_inputs(inp, device=dev)
+    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps)
+    ids, x, mask = d["hash_ids"], d["x"], d["mask"]
+    out = torch.empty_like(x)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for _ in range(args.warmup):
+        layer.forward(ids, x, mask, out=out)
+    torch.cuda.synchronize()
+    st, _ = layer.sync_status()
+    if st != 0:
+        raise RuntimeError(f"engram_forward reported status {st} in warm-up")
+
+    # ---- device-timed steps (inputs resident in HBM)
+    layer.enable_stage_timing(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    stages = []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        layer.forward(ids, x, mask, out=out)
+        ev[i][1].record(stream)
+        stages.append(layer.stage_times())       # waits for this step's last event
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    layer.enable_stage_timing(False)
+
+    # keep the GPU busy a little longer so the clock sampler sees the load
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            layer.forward(ids, x, mask, out=out)
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st, _ = layer.sync_status()
+    if st != 0:
+        raise RuntimeError(f"engram_forward reported status {st}")
+
+    # ---- end to end: pinned host inputs, copies inside the timed region
+    h_ids = inp_pinned(torch, inp.hash_ids)
+    h_x = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
+    h_mask = None if inp.mask is None else torch.from_numpy(inp.mask).pin_memory()
+    h_out = torch.empty(h_x.shape, dtype=torch.int16).pin_memory()
+    d_ids = torch.empty_like(ids)
+    d_x = torch.empty(x.shape, dtype=torch.int16, device=dev)
+    d_mask = None if mask is None else torch.empty_like(mask)
+    d_out = torch.empty_like(d_x)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def e2e_step():
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        if d_mask is not None:
+            d_mask.copy_(h_mask, non_blocking=True)
+        layer.forward(d_ids, d_x, d_mask, out=d_out)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if not np.array_equal(h_out.numpy().view(np.uint16), out.view(torch.int16).cpu().numpy().view(np.uint16)):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
+    h2d = inp.hash_ids.nbytes + inp.x.nbytes + (0 if inp.mask is None else inp.mask.nbytes)
+    d2h = inp.x.nbytes
+
+    # ---- aggregate over ranks
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t[0]), float(t[1])
+    value = world * M * args.steps / (total_ms / 1e3)
+    e2e_value = world * M * args.steps / (e2e_ms / 1e3)
+
+    pk = peaks()
+    splits, ctas = layer.plan(M)
+    gather_ms = statistics.mean(s[0] for s in stages)
+    proj_ms = statistics.mean(s[1] for s in stages)
+    gate_ms = statistics.mean(s[2] for s in stages)
+    pbytes = projection_bytes(w, M)
+    pflops = 2.0 * w.N * w.K * M
+    t_mem = pbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = pflops / (pk["bf16_tflops"] * 1e12)
+    if t_mem >= t_tc:
+        roof = {"bound": "hbm", "achieved": pbytes / (proj_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": pflops / (proj_ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["kernel"] = "wkv_gemm_kernel (tcgen05 projection)"
+    roof["peak_source"] = pk["source"]
+    roof["algorithmic_bytes_per_launch"] = pbytes
+    roof["algorithmic_flops_per_launch"] = pflops
+    roof["avg_launch_ms"] = proj_ms
+
+    lbytes, lflops = algorithmic(w, M)
+    t_roof = max(lbytes / (pk["hbm_gbs"] * 1e9), lflops / (pk["bf16_tflops"] * 1e12))
+    ms_per_step = total_ms / args.steps
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 3 * args.steps,
+        "roofline": roof,
+        "layer_roofline": {"bytes": lbytes, "flops": lflops, "roofline_us": 1e6 * t_roof,
+                           "achieved_us": 1e3 * ms_per_step, "frac": t_roof / (ms_per_step * 1e-3)},
+        "stages_ms": {"gather": gather_ms, "projection": proj_ms, "gate": gate_ms},
+        "gather_gbs": gather_bytes(w, M) / (gather_ms * 1e-3) / 1e9,
+        "plan": {"splits": splits, "ctas": ctas},
+        "clocks": clocks,
+    }
+    layer.close()
+    del table, scale
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        v, el, n, desc = cpu_oracle_run(w, inp, min_seconds=args.cpu_seconds)
+        result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                                  "sample": desc, "seconds": el}
+    return result
+
+
+def inp_pinned(torch, a):
+    return torch.from_numpy(a).pin_memory()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from engram_hashed_gram_gb300 import synth
+    w = synth.workload(int(args.workload) if args.workload.isdigit() else args.workload)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, w, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

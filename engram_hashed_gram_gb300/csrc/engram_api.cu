@@ -1,0 +1,414 @@
+// C ABI of the Engram layer (include/engram.h): argument checks, scratch
+// ownership, the projection's work plan and the launch sequence
+//   gather/dequant -> tcgen05 projection -> gate + residual
+// on the caller's stream.  No step runs on the host.
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/engram.h"
+#include "common.cuh"
+#include "internal.cuh"
+
+using namespace engram;
+
+struct engram_ctx {
+  engram_config cfg;
+  engram_weights w;
+  int device;
+  int num_sms;
+  int32_t K;
+  int32_t N;
+  float* wprod;               // [hc, dim] fp32
+  uint16_t* rows;             // [max_tokens, K] bf16 gathered rows
+  uint16_t* kv;               // [max_tokens, N] bf16
+  float* part;                // [kMaxSplits, part_tokens, N] fp32
+  int64_t part_tokens;
+  unsigned long long* err;    // device [2]
+  CUtensorMap tmW;
+  cudaEvent_t ev[4];          // stage timing (null unless enabled)
+  bool timing;
+};
+
+namespace {
+
+constexpr int kMaxSplits = 8;
+constexpr int64_t kSplitMaxTokens = 128;   // split-K only while one M tile covers the batch
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// bf16 [rows, cols] row-major matrix, box = [box_rows, 64 columns], 128-byte swizzle
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Plan {
+  int32_t splits;
+  int32_t ctas;
+  int32_t m_tiles;
+  int32_t n_tiles;
+  int64_t units;
+};
+
+Plan make_plan(const engram_ctx* c, int64_t M) {
+  Plan p{};
+  p.m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+  p.n_tiles = c->N / kBN;
+  const int32_t kbt = c->K / kBK;
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  auto waves = [&](int64_t units) { return (units + c->num_sms - 1) / c->num_sms; };
+  int32_t best = 1;
+  int64_t best_cost = waves(tiles) * kbt;
+  if (M <= kSplitMaxTokens && M <= c->part_tokens) {
+    const int32_t cand[] = {2, 3, 4, 6, 8};
+    for (int32_t s : cand) {
+      if (s > kMaxSplits || kbt % s != 0) continue;
+      const int64_t cost = waves(tiles * s) * (kbt / s);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = s;
+      }
+    }
+  }
+  p.splits = best;
+  p.units = tiles * best;
+  p.ctas = static_cast<int32_t>(p.units < c->num_sms ? p.units : c->num_sms);
+  return p;
+}
+
+engram_status check_tokens(const engram_ctx* c, int64_t B, int64_t T, int64_t* M) {
+  if (B < 0 || T < 0) return ENGRAM_EINVAL;
+  if (B != 0 && T > INT64_MAX / B) return ENGRAM_EINVAL;
+  *M = B * T;
+  if (*M > c->cfg.max_tokens) return ENGRAM_EINVAL;
+  return ENGRAM_OK;
+}
+
+engram_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ECUDA; }
+
+void mark(engram_ctx* c, int i, cudaStream_t s) {
+  if (c->timing) cudaEventRecord(c->ev[i], s);
+}
+
+void destroy_events(engram_ctx* c) {
+  for (auto& e : c->ev) {
+    if (e != nullptr) cudaEventDestroy(e);
+    e = nullptr;
+  }
+  c->timing = false;
+}
+
+GatherArgs gather_args(const engram_ctx* c, const int64_t* ids, uint16_t* out, int64_t M) {
+  GatherArgs g{};
+  g.ids = ids;
+  g.table = c->w.table;
+  g.scale = c->w.scale;
+  g.out = out;
+  g.rows_total = M * c->cfg.n_cols;
+  g.R = c->cfg.num_rows;
+  g.head_dim = c->cfg.head_dim;
+  g.scale_block = c->cfg.scale_block;
+  g.scale_fmt = c->cfg.scale_fmt;
+  g.check_ids = c->cfg.check_ids;
+  g.err = c->err;
+  return g;
+}
+
+// gathered rows -> projection; writes bf16 kv to kv_out when splits == 1, the
+// fp32 partials to the context otherwise.  Returns the plan used.
+engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint16_t* kv_out, Plan* plan_out,
+                             cudaStream_t stream) {
+  if (cudaSetDevice(c->device) != cudaSuccess) return ENGRAM_ECUDA;
+  GatherArgs g = gather_args(c, ids, c->rows, M);
+  mark(c, 0, stream);
+  if (launch_gather(g, c->num_sms, stream) != cudaSuccess) return ENGRAM_ECUDA;
+  mark(c, 1, stream);
+  CUtensorMap tmA;
+  if (!make_tmap_bf16(&tmA, c->rows, static_cast<uint64_t>(M), static_cast<uint64_t>(c->K), kBM))
+    return ENGRAM_ECUDA;
+  const Plan p = make_plan(c, M);
+  GemmArgs a{};
+  a.M = M;
+  a.N = c->N;
+  a.K = c->K;
+  a.splits = p.splits;
+  a.kb_per_split = (c->K / kBK) / p.splits;
+  a.m_tiles = p.m_tiles;
+  a.n_tiles = p.n_tiles;
+  a.group_m = p.m_tiles < 16 ? p.m_tiles : 16;
+  a.units = p.units;
+  a.out_mode = p.splits == 1 ? kOutBf16 : kOutPartial;
+  a.kv = kv_out;
+  a.part = c->part;
+  a.err = c->err;
+  if (launch_gemm(tmA, c->tmW, a, p.ctas, stream) != cudaSuccess) return ENGRAM_ECUDA;
+  mark(c, 2, stream);
+  *plan_out = p;
+  return ENGRAM_OK;
+}
+
+GateArgs gate_args(const engram_ctx* c, const uint16_t* x, const uint8_t* mask, uint16_t* out, float* gates,
+                   int64_t M) {
+  GateArgs a{};
+  a.x = x;
+  a.mask = mask;
+  a.wprod = c->wprod;
+  a.out = out;
+  a.gates = gates;
+  a.M = M;
+  a.dim = c->cfg.dim;
+  a.hc = c->cfg.hc_mult;
+  a.eps = c->cfg.eps;
+  a.clamp = c->cfg.clamp;
+  a.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c->cfg.dim)));
+  return a;
+}
+
+void free_ctx(engram_ctx* c) {
+  if (c == nullptr) return;
+  destroy_events(c);
+  cudaFree(c->wprod);
+  cudaFree(c->rows);
+  cudaFree(c->kv);
+  cudaFree(c->part);
+  cudaFree(c->err);
+  delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* engram_status_string(engram_status s) {
+  switch (s) {
+    case ENGRAM_OK: return "ok";
+    case ENGRAM_EINVAL: return "invalid argument";
+    case ENGRAM_ENOMEM: return "out of memory";
+    case ENGRAM_ECUDA: return "CUDA error";
+    case ENGRAM_ERANGE: return "hash id outside the table";
+    case ENGRAM_ETIMEOUT: return "kernel wait timed out";
+    case ENGRAM_EUNSUPPORTED: return "unsupported shape or format";
+  }
+  return "unknown status";
+}
+
+int32_t engram_abi_version(void) { return 100; }
+
+engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w) {
+  if (out == nullptr || cfg == nullptr || w == nullptr) return ENGRAM_EINVAL;
+  *out = nullptr;
+  const engram_config& c = *cfg;
+  if (c.dim <= 0 || c.hc_mult <= 0 || c.n_cols <= 0 || c.head_dim <= 0 || c.scale_block <= 0 ||
+      c.num_rows < 0 || c.max_tokens < 0 || !(c.eps >= 0.0f) || !(c.clamp >= 0.0f))
+    return ENGRAM_EINVAL;
+  if (w->table == nullptr || w->scale == nullptr || w->wkv == nullptr || w->q_weight == nullptr ||
+      w->k_weight == nullptr)
+    return ENGRAM_EINVAL;
+  if (!aligned(w->table, 16) || !aligned(w->wkv, 16) || !aligned(w->q_weight, 16) || !aligned(w->k_weight, 16) ||
+      !aligned(w->scale, c.scale_fmt == ENGRAM_SCALE_F32 ? 4 : 1))
+    return ENGRAM_EINVAL;
+  if (c.scale_fmt != ENGRAM_SCALE_F32 && c.scale_fmt != ENGRAM_SCALE_E8M0) return ENGRAM_EUNSUPPORTED;
+  if (c.dim % kBN != 0 || c.dim > 5120 || c.hc_mult > 4) return ENGRAM_EUNSUPPORTED;
+  if (c.head_dim % 16 != 0 || c.head_dim % c.scale_block != 0 || c.scale_block % 16 != 0)
+    return ENGRAM_EUNSUPPORTED;
+  const int64_t K = static_cast<int64_t>(c.n_cols) * c.head_dim;
+  const int64_t N = static_cast<int64_t>(c.dim) * (c.hc_mult + 1);
+  if (K % kBK != 0 || K > (1 << 20) || N > (1 << 24)) return ENGRAM_EUNSUPPORTED;
+
+  engram_ctx* ctx = new (std::nothrow) engram_ctx();
+  if (ctx == nullptr) return ENGRAM_ENOMEM;
+  ctx->cfg = c;
+  ctx->w = *w;
+  ctx->K = static_cast<int32_t>(K);
+  ctx->N = static_cast<int32_t>(N);
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
+    delete ctx;
+    return ENGRAM_ECUDA;
+  }
+  int cc_major = 0, cc_minor = 0;
+  cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, ctx->device);
+  cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
+  if (cc_major != 10 || cc_minor != 3) {   // sm_103a code only
+    delete ctx;
+    return ENGRAM_EUNSUPPORTED;
+  }
+  const int64_t mt = c.max_tokens > 0 ? c.max_tokens : 1;
+  ctx->part_tokens = mt < kSplitMaxTokens ? mt : kSplitMaxTokens;
+  const size_t hcd = static_cast<size_t>(c.hc_mult) * c.dim;
+  bool ok = cudaMalloc(&ctx->wprod, hcd * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&ctx->rows, static_cast<size_t>(mt) * K * 2) == cudaSuccess &&
+            cudaMalloc(&ctx->kv, static_cast<size_t>(mt) * N * 2) == cudaSuccess &&
+            cudaMalloc(&ctx->part, static_cast<size_t>(kMaxSplits) * ctx->part_tokens * N * 4) == cudaSuccess &&
+            cudaMalloc(&ctx->err, 2 * sizeof(unsigned long long)) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_ctx(ctx);
+    return ENGRAM_ENOMEM;
+  }
+  if (cudaMemset(ctx->err, 0, 2 * sizeof(unsigned long long)) != cudaSuccess ||
+      launch_weight_product(w->q_weight, w->k_weight, ctx->wprod, static_cast<int64_t>(hcd), nullptr) !=
+          cudaSuccess ||
+      gemm_prepare() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    free_ctx(ctx);
+    return ENGRAM_ECUDA;
+  }
+  if (!make_tmap_bf16(&ctx->tmW, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN)) {
+    free_ctx(ctx);
+    return ENGRAM_ECUDA;
+  }
+  *out = ctx;
+  return ENGRAM_OK;
+}
+
+void engram_destroy(engram_ctx* ctx) {
+  if (ctx == nullptr) return;
+  cudaSetDevice(ctx->device);
+  cudaDeviceSynchronize();
+  free_ctx(ctx);
+}
+
+engram_status engram_forward(engram_ctx* ctx, const int64_t* hash_ids, const uint16_t* x,
+                             const uint8_t* token_mask, uint16_t* out, int64_t B, int64_t T,
+                             engram_stream_t stream) {
+  if (ctx == nullptr) return ENGRAM_EINVAL;
+  int64_t M;
+  engram_status st = check_tokens(ctx, B, T, &M);
+  if (st != ENGRAM_OK) return st;
+  if (M == 0) return ENGRAM_OK;
+  if (hash_ids == nullptr || x == nullptr || out == nullptr) return ENGRAM_EINVAL;
+  if (!aligned(hash_ids, 8) || !aligned(x, 16) || !aligned(out, 16)) return ENGRAM_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Plan p{};
+  st = run_projection(ctx, hash_ids, M, ctx->kv, &p, s);
+  if (st != ENGRAM_OK) return st;
+  GateArgs g = gate_args(ctx, x, token_mask, out, nullptr, M);
+  if (p.splits == 1) {
+    g.kv = ctx->kv;
+  } else {
+    g.part = ctx->part;
+    g.splits = p.splits;
+  }
+  st = cuda_status(launch_gate(g, s));
+  mark(ctx, 3, s);
+  return st;
+}
+
+engram_status engram_lookup_project(engram_ctx* ctx, const int64_t* hash_ids, uint16_t* kv, int64_t B,
+                                    int64_t T, engram_stream_t stream) {
+  if (ctx == nullptr) return ENGRAM_EINVAL;
+  int64_t M;
+  engram_status st = check_tokens(ctx, B, T, &M);
+  if (st != ENGRAM_OK) return st;
+  if (M == 0) return ENGRAM_OK;
+  if (hash_ids == nullptr || kv == nullptr || !aligned(hash_ids, 8) || !aligned(kv, 16)) return ENGRAM_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Plan p{};
+  st = run_projection(ctx, hash_ids, M, kv, &p, s);
+  if (st != ENGRAM_OK) return st;
+  if (p.splits > 1) st = cuda_status(launch_reduce_partials(ctx->part, p.splits, M, ctx->N, kv, ctx->num_sms, s));
+  mark(ctx, 3, s);
+  return st;
+}
+
+engram_status engram_gate_apply(engram_ctx* ctx, const uint16_t* kv, const uint16_t* x, const uint8_t* token_mask,
+                                uint16_t* out, float* gates, int64_t B, int64_t T, engram_stream_t stream) {
+  if (ctx == nullptr) return ENGRAM_EINVAL;
+  int64_t M;
+  engram_status st = check_tokens(ctx, B, T, &M);
+  if (st != ENGRAM_OK) return st;
+  if (M == 0) return ENGRAM_OK;
+  if (kv == nullptr || x == nullptr || out == nullptr) return ENGRAM_EINVAL;
+  if (!aligned(kv, 16) || !aligned(x, 16) || !aligned(out, 16) || !aligned(gates, 4)) return ENGRAM_EINVAL;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return ENGRAM_ECUDA;
+  GateArgs g = gate_args(ctx, x, token_mask, out, gates, M);
+  g.kv = kv;
+  return cuda_status(launch_gate(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+engram_status engram_lookup(engram_ctx* ctx, const int64_t* hash_ids, uint16_t* rows, int64_t B, int64_t T,
+                            engram_stream_t stream) {
+  if (ctx == nullptr) return ENGRAM_EINVAL;
+  int64_t M;
+  engram_status st = check_tokens(ctx, B, T, &M);
+  if (st != ENGRAM_OK) return st;
+  if (M == 0) return ENGRAM_OK;
+  if (hash_ids == nullptr || rows == nullptr || !aligned(hash_ids, 8) || !aligned(rows, 16)) return ENGRAM_EINVAL;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return ENGRAM_ECUDA;
+  GatherArgs g = gather_args(ctx, hash_ids, rows, M);
+  return cuda_status(launch_gather(g, ctx->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+engram_status engram_sync_status(engram_ctx* ctx, engram_stream_t stream, int64_t* bad_ids) {
+  if (ctx == nullptr) return ENGRAM_EINVAL;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return ENGRAM_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned long long h[2] = {0, 0};
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ENGRAM_ECUDA;
+  if (cudaMemcpy(h, ctx->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ENGRAM_ECUDA;
+  if (cudaMemset(ctx->err, 0, sizeof(h)) != cudaSuccess) return ENGRAM_ECUDA;
+  if (bad_ids != nullptr) *bad_ids = static_cast<int64_t>(h[1]);
+  if (h[0] & kErrTimeout) return ENGRAM_ETIMEOUT;
+  if (h[0] & kErrRange) return ENGRAM_ERANGE;
+  return ENGRAM_OK;
+}
+
+engram_status engram_enable_stage_timing(engram_ctx* ctx, int32_t enable) {
+  if (ctx == nullptr) return ENGRAM_EINVAL;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return ENGRAM_ECUDA;
+  destroy_events(ctx);
+  if (!enable) return ENGRAM_OK;
+  for (auto& e : ctx->ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      destroy_events(ctx);
+      return ENGRAM_ECUDA;
+    }
+  }
+  ctx->timing = true;
+  return ENGRAM_OK;
+}
+
+engram_status engram_stage_times(engram_ctx* ctx, float* ms) {
+  if (ctx == nullptr || ms == nullptr || !ctx->timing) return ENGRAM_EINVAL;
+  if (cudaEventSynchronize(ctx->ev[3]) != cudaSuccess) return ENGRAM_ECUDA;
+  for (int i = 0; i < 3; ++i)
+    if (cudaEventElapsedTime(&ms[i], ctx->ev[i], ctx->ev[i + 1]) != cudaSuccess) return ENGRAM_ECUDA;
+  return ENGRAM_OK;
+}
+
+engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, int32_t* splits, int32_t* ctas) {
+  if (ctx == nullptr || m_tokens < 0) return ENGRAM_EINVAL;
+  const Plan p = make_plan(ctx, m_tokens);
+  if (splits != nullptr) *splits = p.splits;
+  if (ctas != nullptr) *ctas = p.ctas;
+  return ENGRAM_OK;
+}
+
+}  // extern "C"

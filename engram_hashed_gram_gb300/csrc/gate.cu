@@ -1,0 +1,218 @@
+// Steps a5-a8 of the Engram layer (atlas.klimoza.dev "deepseek-v4.1 /
+// engram-second", `Engram.forward`; zhuai.tech "Engram in DeepSeek V4.1 Flash",
+// section "Step 3: Inject memory at the correct layer boundary"):
+//   key[s, d] = kv[s*dim + d], value[d] = kv[hc*dim + d]   (bf16)
+//   rstd[s]   = 1/sqrt(mean_d h^2 + eps) * 1/sqrt(mean_d key^2 + eps)
+//   dot[s]    = (sum_d h * (q_weight*k_weight) * key) * rstd * dim^-0.5
+//   gate[s]   = sigmoid(copysign(sqrt(max(|dot|, clamp)), dot)), 0 if masked
+//   out[s, d] = bf16(h + gate[s] * value[d]); masked tokens copy x bit-for-bit.
+//
+// One CTA per token; thread t owns channels 8t..8t+7 of every stream, so all
+// loads are 16-byte vectors and the token's x, key and value are each read
+// once.  The three per-stream sums are reduced in a fixed order (warp
+// butterflies, then warps in index order): the result does not depend on
+// timing, and the path that reads fp32 split-K partials rounds kv to bf16
+// exactly as the separate reduction kernel does, so the fused layer and
+// lookup_project + gate_apply agree bit-for-bit.
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kMaxHc = 4;
+constexpr int kGateMaxThreads = 640;   // dim / 8 for dim = 5120
+
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// 8 kv values from the fp32 partial sums: summed over the splits in order,
+// then rounded to bf16 (the projection's output type).
+__device__ __forceinline__ void load8_partials(const float* part, int splits, int64_t split_stride, float (&f)[8]) {
+  float4 a = __ldg(reinterpret_cast<const float4*>(part));
+  float4 b = __ldg(reinterpret_cast<const float4*>(part) + 1);
+  for (int s = 1; s < splits; ++s) {
+    const float4* p = reinterpret_cast<const float4*>(part + s * split_stride);
+    const float4 c = __ldg(p), d = __ldg(p + 1);
+    a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+    b.x += d.x; b.y += d.y; b.z += d.z; b.w += d.w;
+  }
+  f[0] = round_bf16(a.x); f[1] = round_bf16(a.y); f[2] = round_bf16(a.z); f[3] = round_bf16(a.w);
+  f[4] = round_bf16(b.x); f[5] = round_bf16(b.y); f[6] = round_bf16(b.z); f[7] = round_bf16(b.w);
+}
+
+template <bool FROM_PARTIALS>
+__global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const GateArgs a) {
+  __shared__ float red[32][3 * kMaxHc];
+  __shared__ float gate_s[kMaxHc];
+
+  grid_dependency_wait();
+  const int64_t m = blockIdx.x;
+  const int t = threadIdx.x;
+  const int D = a.dim;
+  const int HC = a.hc;
+  const int64_t N = static_cast<int64_t>(D) * (HC + 1);
+  const int d0 = 8 * t;
+  const bool active = d0 < D;
+  const uint16_t* xm = a.x + m * HC * D;
+  uint16_t* om = a.out + m * HC * D;
+
+  if (a.mask != nullptr && a.mask[m] == 0) {
+    // "pass through untouched": the streams are copied, the gate is 0
+    if (active && om != xm) {
+      for (int s = 0; s < HC; ++s)
+        *reinterpret_cast<uint4*>(om + s * D + d0) = __ldg(reinterpret_cast<const uint4*>(xm + s * D + d0));
+    }
+    if (a.gates != nullptr && t < HC) a.gates[m * HC + t] = 0.0f;
+    return;
+  }
+
+  float h[kMaxHc][8];
+  float v[8];
+  float sums[3 * kMaxHc];
+#pragma unroll
+  for (int i = 0; i < 3 * kMaxHc; ++i) sums[i] = 0.0f;
+
+  if (active) {
+    const int64_t split_stride = a.M * N;
+#pragma unroll
+    for (int s = 0; s < kMaxHc; ++s) {
+      if (s < HC) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(xm + s * D + d0)), h[s]);
+        float k[8];
+        if (FROM_PARTIALS) {
+          load8_partials(a.part + m * N + s * D + d0, a.splits, split_stride, k);
+        } else {
+          unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + s * D + d0)), k);
+        }
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0) + 1);
+        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          sh = fmaf(h[s][j], h[s][j], sh);
+          sk = fmaf(k[j], k[j], sk);
+          sd = fmaf(h[s][j] * w[j], k[j], sd);
+        }
+        sums[3 * s + 0] = sh;
+        sums[3 * s + 1] = sk;
+        sums[3 * s + 2] = sd;
+      }
+    }
+    if (FROM_PARTIALS) {
+      load8_partials(a.part + m * N + static_cast<int64_t>(HC) * D + d0, a.splits, split_stride, v);
+    } else {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + static_cast<int64_t>(HC) * D + d0)), v);
+    }
+  }
+
+  // block reduction in a fixed order
+#pragma unroll
+  for (int i = 0; i < 3 * kMaxHc; ++i) {
+    float x = sums[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+    sums[i] = x;
+  }
+  const int warp = t >> 5, lane = t & 31;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 3 * kMaxHc; ++i) red[warp][i] = sums[i];
+  }
+  __syncthreads();
+  if (t < HC) {
+    float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+    for (int w = 0; w < nwarps; ++w) {
+      sh += red[w][3 * t + 0];
+      sk += red[w][3 * t + 1];
+      sd += red[w][3 * t + 2];
+    }
+    const float inv_d = 1.0f / static_cast<float>(D);
+    const float rstd = (1.0f / sqrtf(sh * inv_d + a.eps)) * (1.0f / sqrtf(sk * inv_d + a.eps));
+    const float dot = sd * rstd * a.inv_sqrt_dim;
+    const float z = copysignf(sqrtf(fmaxf(fabsf(dot), a.clamp)), dot);
+    const float g = 1.0f / (1.0f + expf(-z));
+    gate_s[t] = g;
+    if (a.gates != nullptr) a.gates[m * HC + t] = g;
+  }
+  __syncthreads();
+
+  if (active) {
+#pragma unroll
+    for (int s = 0; s < kMaxHc; ++s) {
+      if (s < HC) {
+        const float g = gate_s[s];
+        uint4 o;
+        o.x = pack_bf16x2(fmaf(g, v[0], h[s][0]), fmaf(g, v[1], h[s][1]));
+        o.y = pack_bf16x2(fmaf(g, v[2], h[s][2]), fmaf(g, v[3], h[s][3]));
+        o.z = pack_bf16x2(fmaf(g, v[4], h[s][4]), fmaf(g, v[5], h[s][5]));
+        o.w = pack_bf16x2(fmaf(g, v[6], h[s][6]), fmaf(g, v[7], h[s][7]));
+        *reinterpret_cast<uint4*>(om + s * D + d0) = o;
+      }
+    }
+  }
+  grid_launch_dependents();
+}
+
+__global__ void reduce_partials_kernel(const float* __restrict__ part, int splits, int64_t MN,
+                                       uint16_t* __restrict__ kv) {
+  const int64_t n4 = MN >> 2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(part) + i);
+    for (int s = 1; s < splits; ++s) {
+      const float4 c = __ldg(reinterpret_cast<const float4*>(part + s * MN) + i);
+      a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    reinterpret_cast<uint2*>(kv)[i] = o;
+  }
+}
+
+__global__ void weight_product_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                                      float* __restrict__ w, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    w[i] = __fmul_rn(bf16_bits_to_float(q[i]), bf16_bits_to_float(k[i]));
+}
+
+}  // namespace
+
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t stream) {
+  if (a.M == 0) return cudaSuccess;
+  int threads = ((a.dim / 8) + 31) / 32 * 32;
+  if (a.part != nullptr) {
+    gate_residual_kernel<true><<<static_cast<unsigned>(a.M), threads, 0, stream>>>(a);
+  } else {
+    gate_residual_kernel<false><<<static_cast<unsigned>(a.M), threads, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_partials(const float* part, int32_t splits, int64_t M, int32_t N, uint16_t* kv,
+                                   int num_sms, cudaStream_t stream) {
+  const int64_t MN = M * N;
+  if (MN == 0) return cudaSuccess;
+  int64_t blocks = (MN / 4 + 255) / 256;
+  if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+  reduce_partials_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, splits, MN, kv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_product(const uint16_t* q, const uint16_t* k, float* wprod, int64_t n,
+                                  cudaStream_t stream) {
+  weight_product_kernel<<<64, 256, 0, stream>>>(q, k, wprod, n);
+  return cudaGetLastError();
+}
+
+}  // namespace engram

@@ -1,0 +1,96 @@
+// Steps a1-a3 of the Engram layer: id range check, row gather and
+// dequantisation (atlas.klimoza.dev "deepseek-v4.1 / engram-second",
+// `ParallelEngramEmbedding.forward`): for row r = ids[i],
+//   out[i, f] = bf16_rn( fp32(e4m3 code[r, f]) *_rn scale[r, f / scale_block] )
+// and a zero row when r is outside [0, R).
+//
+// One thread owns one 16-byte chunk of a row (16 codes): consecutive threads
+// read consecutive chunks of the same 256-byte row, so each row is one fully
+// used set of 32-byte sectors, and write 32 bytes of bf16 each.  The table is
+// read once with no L1 allocation.  The fp8 -> half conversion is exact and the
+// product is a single fp32 multiply (no FMA contraction), so the result is
+// bit-identical to the definition.
+#include "common.cuh"
+#include "internal.cuh"
+
+namespace engram {
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream_v4(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float e8m0_to_float(uint32_t e) {
+  if (e == 0u) return __uint_as_float(0x00400000u);   // 2^-127, an fp32 subnormal
+  if (e == 255u) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float(e << 23);
+}
+
+// 4 codes (one 32-bit word, lowest byte first) -> 4 bf16 in two words
+__device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& o0, uint32_t& o1) {
+  const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
+  const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+  const float2 f01 = __half22float2(__half2(h01));
+  const float2 f23 = __half22float2(__half2(h23));
+  o0 = pack_bf16x2(__fmul_rn(f01.x, s), __fmul_rn(f01.y, s));
+  o1 = pack_bf16x2(__fmul_rn(f23.x, s), __fmul_rn(f23.y, s));
+}
+
+template <int SCALE_FMT>
+__global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
+  grid_dependency_wait();
+  const int cpr = a.head_dim >> 4;              // 16-byte chunks per row
+  const int nb = a.head_dim / a.scale_block;
+  const int64_t total = a.rows_total * cpr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t row = i / cpr;
+    const int ch = static_cast<int>(i - row * cpr);
+    const int64_t r = __ldg(a.ids + row);
+    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
+    if (r >= 0 && r < a.R) {
+      const uint4 c = ld_stream_v4(a.table + r * a.head_dim + ch * 16);
+      const int blk = (ch * 16) / a.scale_block;
+      float s;
+      if (SCALE_FMT == 0) {
+        s = __ldg(static_cast<const float*>(a.scale) + r * nb + blk);
+      } else {
+        s = e8m0_to_float(__ldg(static_cast<const uint8_t*>(a.scale) + r * nb + blk));
+      }
+      dequant4(c.x, s, lo.x, lo.y);
+      dequant4(c.y, s, lo.z, lo.w);
+      dequant4(c.z, s, hi.x, hi.y);
+      dequant4(c.w, s, hi.z, hi.w);
+    } else if (a.check_ids && ch == 0) {
+      atomicAdd(a.err + 1, 1ull);
+      atomicOr(a.err, kErrRange);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.out + row * a.head_dim + ch * 16);
+    dst[0] = lo;
+    dst[1] = hi;
+  }
+  grid_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream) {
+  const int64_t total = a.rows_total * (a.head_dim >> 4);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // 8 resident CTAs of 256 per SM
+  if (blocks > cap) blocks = cap;
+  if (a.scale_fmt == 0) {
+    gather_dequant_kernel<0><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
+  } else {
+    gather_dequant_kernel<1><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace engram

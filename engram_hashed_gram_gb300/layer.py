@@ -1,0 +1,175 @@
+"""Python binding of the Engram layer's C ABI (include/engram.h).
+
+Argument marshalling only: shapes, dtypes and device pointers of torch tensors
+are checked and handed to libengram.so; every step of the layer runs in the
+library's CUDA kernels on the tensors' device, on the current torch stream
+unless another is given.  PyTorch is used for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import EngramConfig, EngramWeights, check
+
+_U16 = (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtypes, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the layer on {device}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class EngramLayer:
+    """One Engram instance bound to caller-owned device tensors.
+
+    table: uint8 [R, head_dim] e4m3 codes; scale: float32 [R, head_dim/scale_block]
+    (or uint8 E8M0 codes with scale_fmt=SCALE_E8M0); wkv: bf16 [dim*(hc+1),
+    n_cols*head_dim]; q_weight, k_weight: bf16 [hc, dim].  The tensors are
+    referenced, not copied, and are kept alive by this object."""
+
+    def __init__(self, table, scale, wkv, q_weight, k_weight, *, dim=5120, hc_mult=4, n_cols=24, head_dim=256,
+                 scale_block=128, scale_fmt=_lib.SCALE_F32, eps=1e-6, clamp=1e-6, max_tokens=4096,
+                 check_ids=False):
+        dev = table.device
+        if dev.type != "cuda":
+            raise ValueError("the Engram layer runs on a CUDA device only")
+        R = table.shape[0]
+        _need(table, "table", (torch.uint8,), (R, head_dim), dev)
+        _need(scale, "scale", (torch.float32,) if scale_fmt == _lib.SCALE_F32 else (torch.uint8,),
+              (R, head_dim // scale_block), dev)
+        _need(wkv, "wkv", _U16, (dim * (hc_mult + 1), n_cols * head_dim), dev)
+        _need(q_weight, "q_weight", _U16, (hc_mult, dim), dev)
+        _need(k_weight, "k_weight", _U16, (hc_mult, dim), dev)
+        self.device = dev
+        self.dim, self.hc_mult, self.n_cols, self.head_dim = dim, hc_mult, n_cols, head_dim
+        self.N = dim * (hc_mult + 1)
+        self.K = n_cols * head_dim
+        self.max_tokens = max_tokens
+        self._keep = (table, scale, wkv, q_weight, k_weight)
+        self.cfg = EngramConfig(dim=dim, hc_mult=hc_mult, n_cols=n_cols, head_dim=head_dim,
+                                scale_block=scale_block, scale_fmt=scale_fmt, num_rows=R, eps=eps, clamp=clamp,
+                                max_tokens=max_tokens, check_ids=1 if check_ids else 0)
+        w = EngramWeights(table=_ptr(table), scale=_ptr(scale), wkv=_ptr(wkv), q_weight=_ptr(q_weight),
+                          k_weight=_ptr(k_weight))
+        self._ctx = ctypes.c_void_p()
+        self._lib = _lib.engram()
+        with torch.cuda.device(dev):
+            check(self._lib.engram_create(ctypes.byref(self._ctx), ctypes.byref(self.cfg), ctypes.byref(w)),
+                  "engram_create")
+
+    # ------------------------------------------------------------------ calls
+    def _tokens(self, hash_ids):
+        _need(hash_ids, "hash_ids", (torch.int64,), None, self.device)
+        if hash_ids.dim() != 3 or hash_ids.shape[2] != self.n_cols:
+            raise ValueError(f"hash_ids must be [B, T, {self.n_cols}]")
+        return hash_ids.shape[0], hash_ids.shape[1]
+
+    def _mask(self, token_mask, B, T):
+        if token_mask is None:
+            return None
+        if token_mask.dtype == torch.bool:
+            token_mask = token_mask.view(torch.uint8)
+        _need(token_mask, "token_mask", (torch.uint8,), (B, T), self.device)
+        return token_mask
+
+    def forward(self, hash_ids, x, token_mask=None, out=None, stream=None):
+        """out = Engram(x); out may be x (in place)."""
+        B, T = self._tokens(hash_ids)
+        _need(x, "x", _U16, (B, T, self.hc_mult, self.dim), self.device)
+        m = self._mask(token_mask, B, T)
+        if out is None:
+            out = torch.empty_like(x)
+        _need(out, "out", _U16, tuple(x.shape), self.device)
+        check(self._lib.engram_forward(self._ctx, _ptr(hash_ids), _ptr(x), _ptr(m), _ptr(out), B, T,
+                                       _stream(stream)), "engram_forward")
+        return out
+
+    __call__ = forward
+
+    def lookup_project(self, hash_ids, kv=None, stream=None):
+        B, T = self._tokens(hash_ids)
+        if kv is None:
+            kv = torch.empty((B, T, self.N), dtype=torch.bfloat16, device=self.device)
+        _need(kv, "kv", _U16, (B, T, self.N), self.device)
+        check(self._lib.engram_lookup_project(self._ctx, _ptr(hash_ids), _ptr(kv), B, T, _stream(stream)),
+              "engram_lookup_project")
+        return kv
+
+    def gate_apply(self, kv, x, token_mask=None, out=None, gates=None, stream=None):
+        B, T = x.shape[0], x.shape[1]
+        _need(kv, "kv", _U16, (B, T, self.N), self.device)
+        _need(x, "x", _U16, (B, T, self.hc_mult, self.dim), self.device)
+        m = self._mask(token_mask, B, T)
+        if out is None:
+            out = torch.empty_like(x)
+        _need(out, "out", _U16, tuple(x.shape), self.device)
+        if gates is not None:
+            _need(gates, "gates", (torch.float32,), (B, T, self.hc_mult), self.device)
+        check(self._lib.engram_gate_apply(self._ctx, _ptr(kv), _ptr(x), _ptr(m), _ptr(out), _ptr(gates), B, T,
+                                          _stream(stream)), "engram_gate_apply")
+        return out
+
+    def lookup(self, hash_ids, rows=None, stream=None):
+        B, T = self._tokens(hash_ids)
+        if rows is None:
+            rows = torch.empty((B, T, self.K), dtype=torch.bfloat16, device=self.device)
+        _need(rows, "rows", _U16, (B, T, self.K), self.device)
+        check(self._lib.engram_lookup(self._ctx, _ptr(hash_ids), _ptr(rows), B, T, _stream(stream)),
+              "engram_lookup")
+        return rows
+
+    def sync_status(self, stream=None):
+        """(status, bad_ids): waits for the stream, returns and clears the
+        device-detected error."""
+        bad = ctypes.c_int64(0)
+        st = self._lib.engram_sync_status(self._ctx, _stream(stream), ctypes.byref(bad))
+        return st, bad.value
+
+    def plan(self, m_tokens):
+        s, c = ctypes.c_int32(0), ctypes.c_int32(0)
+        check(self._lib.engram_plan(self._ctx, m_tokens, ctypes.byref(s), ctypes.byref(c)), "engram_plan")
+        return s.value, c.value
+
+    def enable_stage_timing(self, enable=True):
+        check(self._lib.engram_enable_stage_timing(self._ctx, 1 if enable else 0), "engram_enable_stage_timing")
+
+    def stage_times(self):
+        """(gather, projection, gate) milliseconds of the last forward /
+        lookup_project call, from CUDA events on its stream."""
+        ms = (ctypes.c_float * 3)()
+        check(self._lib.engram_stage_times(self._ctx, ms), "engram_stage_times")
+        return tuple(ms)
+
+    def close(self):
+        if getattr(self, "_ctx", None) is not None and self._ctx.value:
+            self._lib.engram_destroy(self._ctx)
+            self._ctx = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,175 @@
+/*
+ * engram.h -- C ABI of the Engram conditional-memory layer forward on one
+ * GB300 GPU (sm_103a).
+ *
+ * The layer is the one printed in the code excerpts of atlas.klimoza.dev
+ * "deepseek-v4.1 / engram-second" (classes `Engram` and
+ * `ParallelEngramEmbedding`).  For each token it
+ *   1. reads n_cols ids, each a global row of the table (ids outside [0, R)
+ *      give a zero row, as the single-rank case of the sharded embedding does);
+ *   2. dequantises each row: fp8-e4m3 code widened to fp32, times the fp32 scale
+ *      of its scale_block-channel block (one fp32 rounding), cast to bf16;
+ *   3. flattens the rows to K = n_cols*head_dim values (element c*head_dim + f);
+ *   4. projects through wkv to N = dim*(hc_mult+1) values, fp32 accumulation,
+ *      bf16 result: hc_mult per-stream keys, then one shared value;
+ *   5. per (token, stream): rstd = rsqrt(mean h^2 + eps) * rsqrt(mean key^2 + eps),
+ *      dot = sum(h * q_weight*k_weight * key) * rstd * dim^-0.5,
+ *      gate = sigmoid(copysign(sqrt(max(|dot|, clamp)), dot)), 0 where the
+ *      token mask is False;
+ *   6. out = bf16(h + gate * value) for every stream; a masked token's streams
+ *      are returned bit-for-bit ("pass through untouched").
+ * The split into lookup+projection and gating follows zhuai.tech "Engram in
+ * DeepSeek V4.1 Flash" (section "Run projection early: overlap CPU work with
+ * the GPU"): the lookup and projection depend only on the ids and may run
+ * ahead; only the gating needs the hidden state.
+ *
+ * Conventions for every call
+ *  - Pointers named as device pointers must be device (or managed) memory of
+ *    the current device; the caller owns them and keeps them alive until the
+ *    work queued on `stream` has finished.  The context never frees them.
+ *  - bf16 and fp8 values are passed as their bit patterns (uint16_t, uint8_t).
+ *  - Row-major layouts, no padding: hash_ids [M, n_cols] int64; x and out
+ *    [M, hc_mult, dim]; kv [M, dim*(hc_mult+1)]; rows [M, n_cols*head_dim];
+ *    token_mask [M] uint8 (non-zero = the layer applies) or NULL (all apply);
+ *    M = B*T tokens.
+ *  - Work is queued on `stream` (NULL = the legacy default stream) and runs
+ *    asynchronously.  Argument errors are returned at once and queue nothing.
+ *    Errors the device detects (ids out of range when check_ids is set, a
+ *    pipeline wait that ran out of time) are recorded in the context and
+ *    returned by engram_sync_status().
+ *  - 16-byte alignment is required for x, out, kv, rows and the table; 8 bytes
+ *    for hash_ids and the scales.
+ *  - A context is not thread-safe: calls on one context must be serialised by
+ *    the caller, and calls on one context must not overlap on the GPU (they
+ *    share the context's scratch); use one stream per context.
+ */
+#ifndef ENGRAM_H
+#define ENGRAM_H
+
+#include <stdint.h>
+
+/* Symbols of the shared library (it is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define ENGRAM_API __attribute__((visibility("default")))
+#else
+#define ENGRAM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* engram_stream_t;
+
+typedef enum {
+  ENGRAM_OK = 0,
+  ENGRAM_EINVAL = -1,        /* bad argument: null pointer, size, alignment */
+  ENGRAM_ENOMEM = -2,        /* device or host allocation failed (create only) */
+  ENGRAM_ECUDA = -3,         /* a CUDA runtime call or kernel launch failed */
+  ENGRAM_ERANGE = -4,        /* check_ids: some id was outside [0, num_rows) */
+  ENGRAM_ETIMEOUT = -5,      /* a kernel's bounded wait ran out; its output is invalid */
+  ENGRAM_EUNSUPPORTED = -6   /* shape or format this build does not implement */
+} engram_status;
+
+typedef enum {
+  ENGRAM_SCALE_F32 = 0,      /* one fp32 scale per scale_block channels */
+  ENGRAM_SCALE_E8M0 = 1      /* one E8M0 byte (2^(e-127)) per scale_block channels */
+} engram_scale_fmt;
+
+typedef struct {
+  int32_t dim;          /* per-stream hidden size (5120 in V4.1); multiple of 256, <= 5120 */
+  int32_t hc_mult;      /* residual streams (4 in V4.1); 1..4 */
+  int32_t n_cols;       /* ids per token: (max_ngram_size-1)*n_heads (24 in V4.1) */
+  int32_t head_dim;     /* channels per table row (256 in V4.1); multiple of 16 */
+  int32_t scale_block;  /* channels per scale; divides head_dim, multiple of 16 */
+  int32_t scale_fmt;    /* engram_scale_fmt */
+  int64_t num_rows;     /* R: rows of the table */
+  float eps;            /* added to both mean squares (the V4.1 config's norm_eps is 1e-20) */
+  float clamp;          /* lower clamp of |dot| before the square root (1e-6 in V4.1) */
+  int32_t max_tokens;   /* largest B*T of any later call; sizes the scratch */
+  int32_t check_ids;    /* non-zero: count ids outside [0, R) and report ENGRAM_ERANGE */
+} engram_config;
+
+typedef struct {
+  const uint8_t* table;     /* device, [R, head_dim] fp8-e4m3 codes */
+  const void* scale;        /* device, [R, head_dim/scale_block] fp32 or uint8 E8M0 */
+  const uint16_t* wkv;      /* device, [dim*(hc_mult+1), n_cols*head_dim] bf16, the
+                               Linear's [out, in] weight: keys of stream s at rows
+                               s*dim .. s*dim+dim-1, the value at rows hc_mult*dim .. */
+  const uint16_t* q_weight; /* device, [hc_mult, dim] bf16 */
+  const uint16_t* k_weight; /* device, [hc_mult, dim] bf16 */
+} engram_weights;
+
+typedef struct engram_ctx engram_ctx;
+
+/* Validates the configuration, allocates the context's scratch on the current
+ * device (sized by max_tokens), forms the fp32 product q_weight*k_weight
+ * (used only as a product, per the `Engram` excerpt) and builds the tensor-map
+ * descriptor of wkv.  The weights are referenced, not copied.  Synchronous.
+ * Returns ENGRAM_EINVAL / ENGRAM_EUNSUPPORTED for bad or unsupported shapes,
+ * ENGRAM_ENOMEM if the scratch cannot be allocated, ENGRAM_ECUDA otherwise. */
+ENGRAM_API engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w);
+
+/* Frees the context's scratch (synchronises the device first).  NULL is a no-op. */
+ENGRAM_API void engram_destroy(engram_ctx* ctx);
+
+/* The whole layer (`Engram.forward` with token_mask): out = layer(x).  out may
+ * equal x (in place); otherwise the two must not overlap.  hash_ids, x,
+ * token_mask and out are device pointers.  B*T must not exceed max_tokens;
+ * B*T == 0 queues nothing. */
+ENGRAM_API engram_status engram_forward(engram_ctx* ctx, const int64_t* hash_ids, const uint16_t* x,
+                             const uint8_t* token_mask, uint16_t* out, int64_t B, int64_t T,
+                             engram_stream_t stream);
+
+/* Steps 1-4 only (independent of the hidden state, so they can run ahead on a
+ * side stream): writes kv [B*T, dim*(hc_mult+1)] bf16 to the device buffer kv.
+ * engram_gate_apply() on this kv gives bit-for-bit the result of
+ * engram_forward(). */
+ENGRAM_API engram_status engram_lookup_project(engram_ctx* ctx, const int64_t* hash_ids, uint16_t* kv,
+                                    int64_t B, int64_t T, engram_stream_t stream);
+
+/* Steps 5-6 on a kv produced by engram_lookup_project (or by the caller):
+ * out = layer(x) given kv.  gates (device, [B*T, hc_mult] fp32, 0 on masked
+ * tokens) is written when non-NULL.  out may equal x. */
+ENGRAM_API engram_status engram_gate_apply(engram_ctx* ctx, const uint16_t* kv, const uint16_t* x,
+                                const uint8_t* token_mask, uint16_t* out, float* gates,
+                                int64_t B, int64_t T, engram_stream_t stream);
+
+/* Steps 1-3 only: the gathered, dequantised rows, [B*T, n_cols*head_dim] bf16,
+ * written to the device buffer rows (the `ParallelEngramEmbedding` output,
+ * flattened). */
+ENGRAM_API engram_status engram_lookup(engram_ctx* ctx, const int64_t* hash_ids, uint16_t* rows,
+                            int64_t B, int64_t T, engram_stream_t stream);
+
+/* Waits for `stream`, then returns and clears the device-detected error
+ * recorded by earlier calls on this context: ENGRAM_ERANGE (with check_ids),
+ * ENGRAM_ETIMEOUT, or ENGRAM_OK.  *bad_ids (may be NULL) receives the number of
+ * out-of-range ids counted since the last call. */
+ENGRAM_API engram_status engram_sync_status(engram_ctx* ctx, engram_stream_t stream, int64_t* bad_ids);
+
+/* Split-K factor and CTA count the projection would use for B*T = m_tokens on
+ * this context's device (for tests and benchmarks; queues nothing). */
+ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, int32_t* splits, int32_t* ctas);
+
+/* Stage timing, for benchmarks.  With enable != 0 the context creates CUDA
+ * events and every later engram_forward / engram_lookup_project records one
+ * before the gather and one after each of its kernels on the call's stream;
+ * enable == 0 destroys them.  engram_stage_times() waits for the last
+ * recorded event and writes the durations of the last call's stages in
+ * milliseconds: ms[0] gather + dequantise, ms[1] projection, ms[2] gate and
+ * residual add (or the split-K reduction, for lookup_project). */
+ENGRAM_API engram_status engram_enable_stage_timing(engram_ctx* ctx, int32_t enable);
+ENGRAM_API engram_status engram_stage_times(engram_ctx* ctx, float* ms);
+
+/* Static description of a status code. */
+ENGRAM_API const char* engram_status_string(engram_status s);
+
+/* ABI version of this library: 100 * major + minor. */
+ENGRAM_API int32_t engram_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_H */

@@ -1,0 +1,198 @@
+"""GPU parity of the CUDA path against the oracle, through the C ABI, on the
+tiny table (24 prime ranges above 4096, 100,776 rows): shapes that span one
+and several 128-token tiles with ragged tails, the split-K decode plan and the
+single-pass prefill plan, masks, in-place calls, out-of-range ids and argument
+errors."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from engram_hashed_gram_gb300 import synth
+from engram_hashed_gram_gb300 import synth_device as SD
+from oracle import engram_oracle as O
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from engram_hashed_gram_gb300 import build as B
+    B.build()
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    w = synth.workload("tiny_1x16")
+    table, scale = SD.make_table(w)
+    inp = synth.make_inputs(w)
+    dev = SD.upload_inputs(inp)
+    layer = EngramLayer(table, scale, dev["wkv"], dev["q"], dev["k"], max_tokens=1024)
+    yield dict(w=w, table=table, scale=scale, inp=inp, dev=dev, layer=layer)
+    layer.close()
+
+
+def _inputs(tiny, B, T, mask_frac=0.0, seed=0, bad_ids=0):
+    w = dataclasses.replace(tiny["w"], B=B, T=T)
+    rng = np.random.default_rng([seed, B, T])
+    lengths, offsets = w.layout()
+    ids = synth.make_hash_ids(w, lengths, offsets, rng)
+    if bad_ids:
+        flat = ids.reshape(-1)
+        pos = rng.choice(flat.size, size=bad_ids, replace=False)
+        flat[pos[0::2]] = -1 - rng.integers(0, 1000, size=pos[0::2].size)
+        flat[pos[1::2]] = w.num_rows() + rng.integers(0, 1000, size=pos[1::2].size)
+    x = synth.make_x(w, rng)
+    mask = None
+    if mask_frac > 0:
+        mask = (rng.random((B, T)) >= mask_frac).astype(np.uint8)
+    inp = synth.HostInputs(w=w, hash_ids=ids, x=x, mask=mask, wkv=tiny["inp"].wkv, q=tiny["inp"].q,
+                           k=tiny["inp"].k)
+    return w, inp
+
+
+def _dev(inp):
+    return (torch.from_numpy(inp.hash_ids).cuda(), SD.bits_to_device(inp.x),
+            None if inp.mask is None else torch.from_numpy(inp.mask).cuda())
+
+
+def test_device_table_matches_host_twin(tiny):
+    w = tiny["w"]
+    R = w.num_rows()
+    rows = np.array([0, 1, 2, 17, 4095, 4096, R // 2, R - 2, R - 1])
+    codes, scales = synth.table_rows(w.seed, rows)
+    got_c = tiny["table"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    got_s = tiny["scale"][torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert np.array_equal(got_c, codes)
+    assert np.array_equal(got_s.view(np.uint32), scales.view(np.uint32))
+    # a whole chunk, bit for bit
+    c2, s2 = synth.table_rows(w.seed, np.arange(5000, 9000))
+    assert np.array_equal(tiny["table"][5000:9000].cpu().numpy(), c2)
+    assert np.array_equal(tiny["scale"][5000:9000].cpu().numpy().view(np.uint32), s2.view(np.uint32))
+
+
+@pytest.mark.parametrize("B,T", [(1, 16), (3, 61), (1, 1), (200, 1)])
+def test_lookup_rows_bit_exact(tiny, B, T):
+    w, inp = _inputs(tiny, B, T, bad_ids=6)
+    ids, _, _ = _dev(inp)
+    rows = tiny["layer"].lookup(ids)
+    st, bad = tiny["layer"].sync_status()
+    assert st == 0 and bad == 0          # check_ids is off: no error, zero rows
+    M = B * T
+    cids, codes, scales = P.compact_rows(w, inp.hash_ids.reshape(M, -1))
+    want = O.lookup(cids, codes, scales, w.scale_block)
+    P.assert_bits_equal_nan_aware(SD.device_bits(rows).reshape(M, -1), want, "gathered rows")
+
+
+@pytest.mark.parametrize("B,T,mask_frac", [(1, 16, 0.0), (1, 1, 0.0), (64, 1, 0.0), (2, 100, 0.1),
+                                           (3, 61, 0.3), (300, 1, 0.05)])
+def test_forward_matches_oracle(tiny, B, T, mask_frac):
+    w, inp = _inputs(tiny, B, T, mask_frac)
+    ids, x, mask = _dev(inp)
+    layer = tiny["layer"]
+    out = layer.forward(ids, x, mask)
+    kv = layer.lookup_project(ids)
+    gates = torch.empty((B, T, 4), dtype=torch.float32, device="cuda")
+    out2 = layer.gate_apply(kv, x, mask, gates=gates)
+    st, _ = layer.sync_status()
+    assert st == 0
+    M = B * T
+    ref_out, ref_g, ref_kv = P.oracle_tokens(w, inp, np.arange(M))
+    # the projection: bf16 kv within one bf16 step of the oracle, and rarely off
+    kvg = O.bf16_value(SD.device_bits(kv).reshape(M, -1))
+    kvr = O.bf16_value(ref_kv)
+    far = np.abs(kvg - kvr) > P.bf16_step(kvr)
+    assert not far.any(), f"kv off by more than one bf16 step at {np.argwhere(far)[:5].tolist()} of {far.sum()}"
+    assert np.mean(kvg != kvr) < 0.02
+    s = P.assert_out_close(SD.device_bits(out).reshape(M, 4, -1), ref_out, f"out B={B} T={T}")
+    g = gates.cpu().numpy().reshape(M, 4)
+    assert np.max(np.abs(g - ref_g)) <= P.GATE_TOL
+    # fused == lookup_project + gate_apply, bit for bit
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    print(f"B={B} T={T} plan={layer.plan(M)} {s}")
+
+
+def test_masked_tokens_pass_through_bitwise_in_place(tiny):
+    w, inp = _inputs(tiny, 4, 50, mask_frac=0.5, seed=3)
+    inp.mask[0, 0] = 0
+    ids, x, mask = _dev(inp)
+    x0 = x.clone()
+    x[0, 0, 1, :7] = -0.0
+    x0[0, 0, 1, :7] = -0.0
+    out = tiny["layer"].forward(ids, x, mask, out=x)      # in place
+    torch.cuda.synchronize()
+    off = mask == 0
+    assert int(off.sum()) > 0
+    assert torch.equal(out[off].view(torch.int16), x0[off].view(torch.int16))
+    assert not torch.equal(out[~off].view(torch.int16), x0[~off].view(torch.int16))
+
+
+def test_deterministic_bitwise(tiny):
+    w, inp = _inputs(tiny, 2, 130, mask_frac=0.1, seed=4)
+    ids, x, mask = _dev(inp)
+    a = tiny["layer"].forward(ids, x, mask)
+    b = tiny["layer"].forward(ids, x, mask)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    w2, inp2 = _inputs(tiny, 64, 1, seed=5)
+    ids2, x2, _ = _dev(inp2)
+    c = tiny["layer"].forward(ids2, x2)
+    d = tiny["layer"].forward(ids2, x2)
+    assert torch.equal(c.view(torch.int16), d.view(torch.int16))
+
+
+def test_check_ids_reports_range_errors(tiny):
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    dev = tiny["dev"]
+    layer = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=64,
+                        check_ids=True)
+    w, inp = _inputs(tiny, 2, 8, bad_ids=5, seed=6)
+    ids, x, _ = _dev(inp)
+    rows = layer.lookup(ids)
+    st, bad = layer.sync_status()
+    assert st == -4 and bad == 5
+    st, bad = layer.sync_status()
+    assert st == 0 and bad == 0           # cleared
+    flat = inp.hash_ids.reshape(-1)
+    zero = (flat < 0) | (flat >= w.num_rows())
+    r = SD.device_bits(rows).reshape(-1, 256)
+    assert np.all(r[zero] == 0) and np.any(r[~zero] != 0)
+    layer.forward(ids, x)
+    st, bad = layer.sync_status()
+    assert st == -4 and bad == 5
+    layer.close()
+
+
+def test_argument_errors_queue_nothing(tiny):
+    import ctypes
+    from engram_hashed_gram_gb300 import _lib
+    lib = _lib.engram()
+    ctx = tiny["layer"]._ctx
+    w, inp = _inputs(tiny, 1, 4)
+    ids, x, _ = _dev(inp)
+    out = torch.empty_like(x)
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.engram_forward(None, ids.data_ptr(), x.data_ptr(), None, out.data_ptr(), 1, 4, s) == -1
+    assert lib.engram_forward(ctx, None, x.data_ptr(), None, out.data_ptr(), 1, 4, s) == -1
+    assert lib.engram_forward(ctx, ids.data_ptr(), x.data_ptr() + 2, None, out.data_ptr(), 1, 4, s) == -1
+    assert lib.engram_forward(ctx, ids.data_ptr(), x.data_ptr(), None, out.data_ptr(), 1, 1025, s) == -1
+    assert lib.engram_forward(ctx, ids.data_ptr(), x.data_ptr(), None, out.data_ptr(), -1, 4, s) == -1
+    assert lib.engram_forward(ctx, ids.data_ptr(), x.data_ptr(), None, out.data_ptr(), 0, 4, s) == 0
+    # an unsupported shape is refused at create
+    cfg = _lib.EngramConfig(dim=5000, hc_mult=4, n_cols=24, head_dim=256, scale_block=128, scale_fmt=0,
+                            num_rows=10, eps=1e-6, clamp=1e-6, max_tokens=8, check_ids=0)
+    wt = _lib.EngramWeights(table=tiny["table"].data_ptr(), scale=tiny["scale"].data_ptr(),
+                            wkv=tiny["dev"]["wkv"].data_ptr(), q_weight=tiny["dev"]["q"].data_ptr(),
+                            k_weight=tiny["dev"]["k"].data_ptr())
+    h = ctypes.c_void_p()
+    assert lib.engram_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(wt)) == -6
+    assert tiny["layer"].sync_status()[0] == 0
+
+
+def test_empty_batch_is_a_no_op(tiny):
+    layer = tiny["layer"]
+    ids = torch.empty((0, 5, 24), dtype=torch.int64, device="cuda")
+    x = torch.empty((0, 5, 4, 5120), dtype=torch.bfloat16, device="cuda")
+    out = layer.forward(ids, x)
+    assert out.shape == x.shape
+    assert layer.sync_status()[0] == 0
