@@ -224,7 +224,8 @@ def config_of(w):
     return {"workload": w.name, "B": w.B, "T": w.T, "tokens": w.M, "dim": w.dim, "hc_mult": w.hc_mult,
             "n_cols": w.n_cols, "head_dim": w.head_dim, "table_rows": w.num_rows(),
             "table_gb": round(w.num_rows() * w.head_dim / 1e9, 2), "hash_ids": w.ids, "mask": w.mask,
-            "wkv": "bf16 [25600, 6144]", "l2": "flushed between timed steps (256 MB write)"}
+            "prime_base": w.prime_base, "wkv": "bf16 [25600, 6144]",
+            "l2": "flushed between timed steps (256 MB write)"}
 
 
 def run_ours(args, w, rank, world, local_rank):
@@ -393,12 +394,19 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prime-base", type=int, default=None,
+                    help="profiling only: build the table from the 24 primes above this base instead of the "
+                         "workload's (the projection and gate kernels do the same work; the gather reads a "
+                         "smaller table)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
     from engram_hashed_gram_gb300 import synth
     w = synth.workload(int(args.workload) if args.workload.isdigit() else args.workload)
+    if args.prime_base is not None:
+        import dataclasses
+        w = dataclasses.replace(w, prime_base=args.prime_base, prime_skip=0)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -25,6 +25,19 @@ def bf16_step(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, np.maximum(e - 8, -133))
 
 
+def kv_bound(e_bits, wkv_bits, kv_ref_bits, K: int, splits: int = 3):
+    """Per-element bound on |gpu kv - oracle kv|: one bf16 step at the oracle
+    value plus the fp32 dot-product error bound gamma_n * sum_k |e_k W_jk|
+    (Higham, "Accuracy and Stability of Numerical Algorithms", section 3.1),
+    with n = K/16 accumulator additions of 16-product MMA partials, 16 more for
+    the partial itself, and the split-K additions."""
+    n = K // 16 + 16 + splits
+    u = 2.0 ** -24
+    gamma = n * u / (1 - n * u)
+    absdot = np.abs(O.bf16_value(e_bits)) @ np.abs(O.bf16_value(wkv_bits)).T
+    return bf16_step(O.bf16_value(kv_ref_bits)) + gamma * absdot
+
+
 def compare_out(gpu_bits, ref_bits):
     g = O.bf16_value(gpu_bits).ravel()
     r = O.bf16_value(ref_bits).ravel()
@@ -59,6 +72,67 @@ def assert_bits_equal_nan_aware(a, b, what=""):
     assert bad.size == 0, f"{what}: {bad.size} bit mismatches, first at {bad[:5]}: {a.ravel()[bad[:5]]} vs {b.ravel()[bad[:5]]}"
 
 
+ILL_DOT = 1e-2   # |dot| below which the gate's sensitivity sigma'(z)/(2 sqrt|dot|) exceeds 1.25
+
+
+def check_layer(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, gpu_out, gpu_gates, gpu_kv,
+                what: str = ""):
+    """Stage-wise parity of the sampled tokens `tok`; returns a summary dict.
+
+    1. kv (projection) against the oracle's kv, element by element, within one
+       bf16 step plus the fp32 dot-product error bound (kv_bound).
+    2. gates and output against the oracle's gate and residual steps fed the
+       GPU's own kv: gates within GATE_TOL, output within max(ABS_TOL, one bf16
+       step) per element and REL_L2_TOL overall.  Same inputs, so this is the
+       strict check of the gate and residual kernels.
+    3. end to end against the oracle from the ids: relative L2 within
+       REL_L2_TOL; every element within max(ABS_TOL, one bf16 step) and every
+       gate within GATE_TOL, except on (token, stream) pairs whose oracle
+       |dot| < ILL_DOT, where the gate's sensitivity to dot exceeds 1.25 and a
+       one-step kv difference (step 1) legitimately moves the gate by more;
+       such pairs must stay under 2% of the pairs, with gate error <= 0.05."""
+    M = len(tok)
+    hc, D = w.hc_mult, w.dim
+    ref_out, ref_g, ref_kv = oracle_tokens(w, inp, tok)
+    x = inp.x.reshape(w.M, hc, D)[tok]
+    mask = None if inp.mask is None else inp.mask.reshape(w.M)[tok]
+    gpu_out = np.asarray(gpu_out, dtype=np.uint16).reshape(M, hc, D)
+    gpu_gates = np.asarray(gpu_gates, dtype=np.float64).reshape(M, hc)
+    gpu_kv = np.asarray(gpu_kv, dtype=np.uint16).reshape(M, -1)
+    # 1. projection
+    bound = kv_bound(oracle_rows(w, inp, tok), inp.wkv, ref_kv, w.K)
+    kv_err = np.abs(O.bf16_value(gpu_kv) - O.bf16_value(ref_kv))
+    far = kv_err > bound
+    assert not far.any(), f"{what}: kv outside the bound at {np.argwhere(far)[:5].tolist()} ({far.sum()})"
+    # 2. gate + residual on identical kv
+    g_same = O.gates(gpu_kv, x, inp.q, inp.k, mask, w.eps)
+    out_same = O.residual(gpu_kv, x, g_same, mask)
+    gate_err_same = float(np.max(np.abs(gpu_gates - g_same)))
+    assert gate_err_same <= GATE_TOL, f"{what}: gate error {gate_err_same} on identical kv"
+    s2 = compare_out(gpu_out, out_same)
+    assert s2["ok"], f"{what}: output vs oracle on identical kv: {s2}"
+    # 3. end to end
+    s3 = compare_out(gpu_out, ref_out)
+    assert s3["rel_l2"] <= REL_L2_TOL, f"{what}: end-to-end rel L2 {s3}"
+    with np.errstate(divide="ignore"):
+        z = np.log(ref_g) - np.log1p(-ref_g)
+    ill = (z * z < ILL_DOT)
+    if mask is not None:
+        ill &= mask.reshape(M, 1).astype(bool)
+    g = O.bf16_value(gpu_out)
+    r = O.bf16_value(ref_out)
+    elem_bad = np.abs(g - r) > np.maximum(ABS_TOL, bf16_step(r))
+    pair_bad = elem_bad.any(axis=-1) | (np.abs(gpu_gates - ref_g) > GATE_TOL)
+    unexplained = pair_bad & ~ill
+    assert not unexplained.any(), (f"{what}: end-to-end mismatch on well-conditioned pairs "
+                                   f"{np.argwhere(unexplained)[:5].tolist()}")
+    assert ill.mean() <= 0.02, f"{what}: {ill.mean():.3%} of pairs ill-conditioned"
+    assert np.max(np.abs(gpu_gates - ref_g)) <= 0.05
+    return {"kv_frac_diff": float((kv_err > 0).mean()), "gate_err_same_kv": gate_err_same,
+            "out_same_kv": s2, "end_to_end": s3, "gate_err_e2e": float(np.max(np.abs(gpu_gates - ref_g))),
+            "ill_pairs": int(ill.sum()), "ill_pairs_off": int((pair_bad & ill).sum()), "pairs": int(ill.size)}
+
+
 def compact_rows(w: synth.Workload, ids: np.ndarray, seed: int | None = None):
     """Regenerates only the table rows that `ids` reference (the full table may
     be ~100 GB) and remaps the ids onto that compact table; ids outside
@@ -76,6 +150,13 @@ def compact_rows(w: synth.Workload, ids: np.ndarray, seed: int | None = None):
     out = np.full(ids.shape, -1, dtype=np.int64)
     out[valid] = np.searchsorted(uniq, ids[valid])
     return out, codes, scales
+
+
+def oracle_rows(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray) -> np.ndarray:
+    """Oracle gathered rows (bf16 bits [n, K]) of the tokens `tok`."""
+    ids = inp.hash_ids.reshape(w.M, w.n_cols)[tok]
+    cids, codes, scales = compact_rows(w, ids)
+    return O.lookup(cids, codes, scales, w.scale_block)
 
 
 def oracle_tokens(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, eps: float | None = None):

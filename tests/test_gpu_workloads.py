@@ -1,0 +1,75 @@
+"""Parity at the benchmark workloads' full sizes, in the launch configuration
+the benchmark times (one engram_forward over the whole batch):
+
+  decode_64x1          B=64,   T=1,    25,169,534 rows (6.4 GB)
+  prefill_1x4096_zipf  B=1,    T=4096, 402,659,764 rows (103 GB), Zipf ids, 10% masked span
+  decode_512x1_skew    B=512,  T=1,    100,667,472 rows (25.8 GB), hot-set ids, near-zero streams
+  full_2x8192          B=2,    T=8192, 384,016,682 rows (98.3 GB), 5% masked
+
+The table is filled on the device by the generator's twin; the oracle
+regenerates only the rows of the sampled tokens.  Sampled tokens are checked
+element by element; properties that hold at any size are checked on every
+token: masked tokens pass through bit-for-bit, the fused call equals
+lookup_project + gate_apply bit-for-bit, and a second run is bit-identical."""
+import numpy as np
+import pytest
+import torch
+
+from engram_hashed_gram_gb300 import synth
+from engram_hashed_gram_gb300 import synth_device as SD
+from oracle import engram_oracle as O
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+WORKLOADS = ["decode_64x1", "prefill_1x4096_zipf", "decode_512x1_skew", "full_2x8192"]
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_workload_parity(name):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from engram_hashed_gram_gb300 import build as B
+    B.build()
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    w = synth.workload(name)
+    M = w.M
+    inp = synth.make_inputs(w)
+    table, scale = SD.make_table(w)
+    d = SD.upload_inputs(inp)
+    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps)
+    try:
+        ids, x, mask = d["hash_ids"], d["x"], d["mask"]
+        out = layer.forward(ids, x, mask)
+        out_again = layer.forward(ids, x, mask)
+        kv = layer.lookup_project(ids)
+        gates = torch.empty((w.B, w.T, w.hc_mult), dtype=torch.float32, device="cuda")
+        out_split = layer.gate_apply(kv, x, mask, gates=gates)
+        st, _ = layer.sync_status()
+        assert st == 0
+        assert torch.equal(out.view(torch.int16), out_again.view(torch.int16)), "run-to-run"
+        assert torch.equal(out.view(torch.int16), out_split.view(torch.int16)), "fused vs split"
+        if mask is not None:
+            off = mask == 0
+            assert int(off.sum()) > 0
+            assert torch.equal(out[off].view(torch.int16), x[off].view(torch.int16)), "masked pass-through"
+            assert torch.all(gates[off] == 0)
+
+        rng = np.random.default_rng([w.seed, 99])
+        must = [M // 2, (M // 128) * 128, (M // 128) * 128 - 1]
+        if inp.mask is not None:
+            off_idx = np.flatnonzero(inp.mask.reshape(-1) == 0)
+            must += list(off_idx[:2]) + list(off_idx[-2:])
+        tok = P.sample_tokens(M, 40, rng, must)
+        tok_t = torch.from_numpy(tok).cuda()
+        summary = P.check_layer(w, inp, tok, SD.device_bits(out.reshape(M, w.hc_mult, w.dim)[tok_t]),
+                                gates.reshape(M, w.hc_mult)[tok_t].cpu().numpy(),
+                                SD.device_bits(kv.reshape(M, -1)[tok_t]), name)
+        rows = layer.lookup(ids.reshape(M, 1, w.n_cols)[tok_t])
+        P.assert_bits_equal_nan_aware(SD.device_bits(rows).reshape(len(tok), -1), P.oracle_rows(w, inp, tok),
+                                      "rows")
+        print(f"{name}: sampled {len(tok)} tokens, plan={layer.plan(M)}, {summary}")
+    finally:
+        layer.close()
+        del table, scale, d
+        torch.cuda.empty_cache()
