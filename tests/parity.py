@@ -72,9 +72,6 @@ def assert_bits_equal_nan_aware(a, b, what=""):
     assert bad.size == 0, f"{what}: {bad.size} bit mismatches, first at {bad[:5]}: {a.ravel()[bad[:5]]} vs {b.ravel()[bad[:5]]}"
 
 
-ILL_DOT = 1e-2   # |dot| below which the gate's sensitivity sigma'(z)/(2 sqrt|dot|) exceeds 1.25
-
-
 def check_layer(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, gpu_out, gpu_gates, gpu_kv,
                 what: str = ""):
     """Stage-wise parity of the sampled tokens `tok`; returns a summary dict.
@@ -86,11 +83,13 @@ def check_layer(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, gpu_o
        step) per element and REL_L2_TOL overall.  Same inputs, so this is the
        strict check of the gate and residual kernels.
     3. end to end against the oracle from the ids: relative L2 within
-       REL_L2_TOL; every element within max(ABS_TOL, one bf16 step) and every
-       gate within GATE_TOL, except on (token, stream) pairs whose oracle
-       |dot| < ILL_DOT, where the gate's sensitivity to dot exceeds 1.25 and a
-       one-step kv difference (step 1) legitimately moves the gate by more;
-       such pairs must stay under 2% of the pairs, with gate error <= 0.05."""
+       REL_L2_TOL, and each gate / output element within its stage-2 tolerance
+       plus the change the oracle itself shows between its own kv and the GPU's
+       (the triangle inequality: the part of the difference that the bounded kv
+       difference of step 1 causes through the exact gate).  Near dot = 0 the
+       signed square root's slope sigma'(z)/(2 sqrt|dot|) amplifies that part,
+       so it is reported (pairs with an end-to-end gate difference above
+       GATE_TOL) and capped: at most 2% of the pairs, gate difference <= 0.05."""
     M = len(tok)
     hc, D = w.hc_mult, w.dim
     ref_out, ref_g, ref_kv = oracle_tokens(w, inp, tok)
@@ -114,23 +113,21 @@ def check_layer(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, gpu_o
     # 3. end to end
     s3 = compare_out(gpu_out, ref_out)
     assert s3["rel_l2"] <= REL_L2_TOL, f"{what}: end-to-end rel L2 {s3}"
-    with np.errstate(divide="ignore"):
+    gate_e2e = np.abs(gpu_gates - ref_g)
+    gate_kv = np.abs(g_same - ref_g)
+    assert np.all(gate_e2e <= GATE_TOL + gate_kv), f"{what}: end-to-end gate difference not explained by kv"
+    g, r, rs = O.bf16_value(gpu_out), O.bf16_value(ref_out), O.bf16_value(out_same)
+    out_bad = np.abs(g - r) > np.maximum(ABS_TOL, bf16_step(rs)) + np.abs(rs - r)
+    assert not out_bad.any(), (f"{what}: end-to-end output difference not explained by kv at "
+                               f"{np.argwhere(out_bad)[:5].tolist()}")
+    amplified = gate_e2e > GATE_TOL
+    assert amplified.mean() <= 0.02 and gate_e2e.max() <= 0.05, f"{what}: gate {gate_e2e.max()}"
+    with np.errstate(divide="ignore", invalid="ignore"):
         z = np.log(ref_g) - np.log1p(-ref_g)
-    ill = (z * z < ILL_DOT)
-    if mask is not None:
-        ill &= mask.reshape(M, 1).astype(bool)
-    g = O.bf16_value(gpu_out)
-    r = O.bf16_value(ref_out)
-    elem_bad = np.abs(g - r) > np.maximum(ABS_TOL, bf16_step(r))
-    pair_bad = elem_bad.any(axis=-1) | (np.abs(gpu_gates - ref_g) > GATE_TOL)
-    unexplained = pair_bad & ~ill
-    assert not unexplained.any(), (f"{what}: end-to-end mismatch on well-conditioned pairs "
-                                   f"{np.argwhere(unexplained)[:5].tolist()}")
-    assert ill.mean() <= 0.02, f"{what}: {ill.mean():.3%} of pairs ill-conditioned"
-    assert np.max(np.abs(gpu_gates - ref_g)) <= 0.05
     return {"kv_frac_diff": float((kv_err > 0).mean()), "gate_err_same_kv": gate_err_same,
-            "out_same_kv": s2, "end_to_end": s3, "gate_err_e2e": float(np.max(np.abs(gpu_gates - ref_g))),
-            "ill_pairs": int(ill.sum()), "ill_pairs_off": int((pair_bad & ill).sum()), "pairs": int(ill.size)}
+            "out_same_kv": s2, "end_to_end": s3, "gate_err_e2e": float(gate_e2e.max()),
+            "pairs_gate_over_tol": int(amplified.sum()), "pairs": int(amplified.size),
+            "min_abs_dot_of_those": float(np.min(z[amplified] ** 2)) if amplified.any() else None}
 
 
 def compact_rows(w: synth.Workload, ids: np.ndarray, seed: int | None = None):
