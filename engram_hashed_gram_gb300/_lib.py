@@ -21,6 +21,9 @@ ENGRAM_ERANGE = -4
 ENGRAM_ETIMEOUT = -5
 ENGRAM_EUNSUPPORTED = -6
 
+NOALLOC_MAX_TOKENS = 64          # ENGRAM_NOALLOC_MAX_TOKENS
+NOALLOC_SCRATCH_BYTES = 20529408  # ENGRAM_NOALLOC_SCRATCH_BYTES
+
 SCALE_F32 = 0
 SCALE_E8M0 = 1
 
@@ -62,6 +65,8 @@ ENGRAM_FUNCS = {
     "engram_lookup": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p]),
     "engram_sync_status": (c_int32, [c_void_p, c_void_p, POINTER(c_int64)]),
     "engram_plan": (c_int32, [c_void_p, c_int64, POINTER(c_int32), POINTER(c_int32)]),
+    "engram_forward_noalloc": (c_int32, [POINTER(EngramConfig), POINTER(EngramWeights), c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_int64, c_int64, c_void_p]),
     "engram_enable_stage_timing": (c_int32, [c_void_p, c_int32]),
     "engram_stage_times": (c_int32, [c_void_p, POINTER(c_float)]),
     "engram_status_string": (c_char_p, [c_int32]),

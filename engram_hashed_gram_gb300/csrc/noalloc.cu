@@ -1,0 +1,216 @@
+// engram_forward_noalloc: the whole layer for small batches (at most
+// ENGRAM_NOALLOC_MAX_TOKENS tokens) with no context and no allocation.
+//
+// Some callers cannot allocate device memory: a serving engine that reserves
+// nearly all of HBM up front for weights and its KV cache and routes every
+// other byte through its own allocator, or a plugin whose host process owns the
+// GPU's memory budget, cannot let a library call cudaMalloc (and could not
+// accept the failure or the implicit synchronisation it may bring).  For them
+// this entry point keeps its scratch -- the gathered rows, the split-K partial
+// sums (or the bf16 kv), q_weight*k_weight and the device error word -- in one
+// file-scope static __device__ array, which the CUDA driver places in device
+// memory when it loads this module on a device; every device that loads it
+// keeps those bytes until the process exits.
+//
+// The kernels are the same as engram_forward's (gather/dequant, tcgen05
+// projection, gate + residual); only where their scratch lives differs.
+#include <cmath>
+#include <mutex>
+
+#include "../../include/engram.h"
+#include "common.cuh"
+#include "internal.cuh"
+
+using namespace engram;
+
+namespace {
+
+constexpr int64_t kMaxTokens = ENGRAM_NOALLOC_MAX_TOKENS;
+constexpr int64_t kMaxK = 6144;           // n_cols * head_dim
+constexpr int64_t kMaxN = 25600;          // dim * (hc_mult + 1)
+constexpr int64_t kMaxHcDim = 4 * 5120;   // hc_mult * dim
+constexpr int32_t kMaxSplits = 3;
+
+constexpr size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+constexpr size_t kErrBytes = 256;
+constexpr size_t kWprodBytes = align256(kMaxHcDim * sizeof(float));
+constexpr size_t kRowsBytes = align256(kMaxTokens * kMaxK * 2);
+constexpr size_t kPartBytes = align256(size_t(kMaxSplits) * kMaxTokens * kMaxN * sizeof(float));
+constexpr size_t kScratchBytes = kErrBytes + kWprodBytes + kRowsBytes + kPartBytes;
+static_assert(kScratchBytes == ENGRAM_NOALLOC_SCRATCH_BYTES, "header and implementation disagree");
+
+// The scratch.  In host code this name is only a stand-in and must not be
+// handed to a kernel; the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned char* g_dev_scratch[kMaxDevices] = {};
+
+// Device address of g_scratch on device `dev` (which must be current), looked
+// up once per device: the first call on a device does this set-up.
+cudaError_t scratch_address(int dev, unsigned char** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_dev_scratch[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess) return e;
+    g_dev_scratch[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_dev_scratch[dev];
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const engram_weights* w,
+                                                const int64_t* hash_ids, const uint16_t* x,
+                                                const uint8_t* token_mask, uint16_t* out, int64_t B, int64_t T,
+                                                engram_stream_t stream) {
+  if (cfg == nullptr || w == nullptr) return ENGRAM_EINVAL;
+  const engram_config& c = *cfg;
+  if (B < 0 || T < 0 || (B != 0 && T > INT64_MAX / B)) return ENGRAM_EINVAL;
+  const int64_t M = B * T;
+  if (M > kMaxTokens) return ENGRAM_EINVAL;   // the static scratch holds ENGRAM_NOALLOC_MAX_TOKENS tokens
+  if (c.dim <= 0 || c.hc_mult <= 0 || c.n_cols <= 0 || c.head_dim <= 0 || c.scale_block <= 0 || c.num_rows < 0 ||
+      !(c.eps >= 0.0f) || !(c.clamp >= 0.0f))
+    return ENGRAM_EINVAL;
+  if (c.scale_fmt != ENGRAM_SCALE_F32 && c.scale_fmt != ENGRAM_SCALE_E8M0) return ENGRAM_EUNSUPPORTED;
+  if (c.dim % kBN != 0 || c.dim > 5120 || c.hc_mult > 4 || c.head_dim % 16 != 0 || c.head_dim % c.scale_block != 0 ||
+      c.scale_block % 16 != 0)
+    return ENGRAM_EUNSUPPORTED;
+  const int64_t K = static_cast<int64_t>(c.n_cols) * c.head_dim;
+  const int64_t N = static_cast<int64_t>(c.dim) * (c.hc_mult + 1);
+  if (K % kBK != 0 || K > kMaxK || N > kMaxN) return ENGRAM_EUNSUPPORTED;
+  if (M == 0) return ENGRAM_OK;
+  if (w->table == nullptr || w->scale == nullptr || w->wkv == nullptr || w->q_weight == nullptr ||
+      w->k_weight == nullptr || hash_ids == nullptr || x == nullptr || out == nullptr)
+    return ENGRAM_EINVAL;
+  if (!aligned(w->table, 16) || !aligned(w->wkv, 16) || !aligned(w->q_weight, 2) || !aligned(w->k_weight, 2) ||
+      !aligned(w->scale, c.scale_fmt == ENGRAM_SCALE_F32 ? 4 : 1) || !aligned(hash_ids, 8) || !aligned(x, 16) ||
+      !aligned(out, 16))
+    return ENGRAM_EINVAL;
+
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ENGRAM_ECUDA;
+  if (major != 10 || minor != 3) return ENGRAM_EUNSUPPORTED;
+  unsigned char* base = nullptr;
+  if (scratch_address(dev, &base) != cudaSuccess) return ENGRAM_ECUDA;
+  auto* err = reinterpret_cast<unsigned long long*>(base);
+  auto* wprod = reinterpret_cast<float*>(base + kErrBytes);
+  auto* rows = reinterpret_cast<uint16_t*>(base + kErrBytes + kWprodBytes);
+  auto* part = reinterpret_cast<float*>(base + kErrBytes + kWprodBytes + kRowsBytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // the split-K factor: engram_forward's rule, restricted to <= kMaxSplits
+  const int32_t m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+  const int32_t n_tiles = static_cast<int32_t>(N / kBN);
+  const int32_t kbt = static_cast<int32_t>(K / kBK);
+  const int64_t tiles = static_cast<int64_t>(m_tiles) * n_tiles;
+  auto waves = [&](int64_t u) { return (u + sms - 1) / sms; };
+  int32_t splits = 1;
+  int64_t best = waves(tiles) * kbt;
+  for (int32_t sp = 2; sp <= kMaxSplits; ++sp) {
+    if (kbt % sp != 0) continue;
+    const int64_t cost = waves(tiles * sp) * (kbt / sp);
+    if (cost < best) {
+      best = cost;
+      splits = sp;
+    }
+  }
+
+  // the error word is the only scratch that must start at zero; the rest is
+  // overwritten before it is read
+  if (cudaMemsetAsync(err, 0, 2 * sizeof(unsigned long long), s) != cudaSuccess) return ENGRAM_ECUDA;
+  if (launch_weight_product(w->q_weight, w->k_weight, wprod, static_cast<int64_t>(c.hc_mult) * c.dim, s) !=
+      cudaSuccess)
+    return ENGRAM_ECUDA;
+
+  GatherArgs g{};
+  g.ids = hash_ids;
+  g.table = w->table;
+  g.scale = w->scale;
+  g.out = rows;
+  g.rows_total = M * c.n_cols;
+  g.R = c.num_rows;
+  g.head_dim = c.head_dim;
+  g.scale_block = c.scale_block;
+  g.scale_fmt = c.scale_fmt;
+  g.check_ids = 0;
+  g.err = err;
+  if (launch_gather(g, sms, s) != cudaSuccess) return ENGRAM_ECUDA;
+
+  CUtensorMap tmA, tmB;
+  if (!tmap_bf16(&tmA, rows, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM) ||
+      !tmap_bf16(&tmB, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN))
+    return ENGRAM_ECUDA;
+  GemmArgs a{};
+  a.M = M;
+  a.N = static_cast<int32_t>(N);
+  a.K = static_cast<int32_t>(K);
+  a.splits = splits;
+  a.kb_per_split = kbt / splits;
+  a.m_tiles = m_tiles;
+  a.n_tiles = n_tiles;
+  a.group_m = m_tiles;
+  a.units = tiles * splits;
+  a.out_mode = splits == 1 ? kOutBf16 : kOutPartial;
+  a.kv = reinterpret_cast<uint16_t*>(part);   // splits == 1: bf16 kv in the partials' space
+  a.part = part;
+  a.err = err;
+  if (gemm_prepare() != cudaSuccess) return ENGRAM_ECUDA;
+  const int ctas = static_cast<int>(a.units < sms ? a.units : sms);
+  if (launch_gemm(tmA, tmB, a, ctas, s) != cudaSuccess) return ENGRAM_ECUDA;
+
+  GateArgs ga{};
+  ga.x = x;
+  ga.mask = token_mask;
+  ga.wprod = wprod;
+  ga.out = out;
+  ga.gates = nullptr;
+  ga.M = M;
+  ga.dim = c.dim;
+  ga.hc = c.hc_mult;
+  ga.eps = c.eps;
+  ga.clamp = c.clamp;
+  ga.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.dim)));
+  if (splits == 1) {
+    ga.kv = reinterpret_cast<const uint16_t*>(part);
+  } else {
+    ga.part = part;
+    ga.splits = splits;
+  }
+  return launch_gate(ga, s) == cudaSuccess ? ENGRAM_OK : ENGRAM_ECUDA;
+}

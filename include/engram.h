@@ -162,6 +162,44 @@ ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, in
 ENGRAM_API engram_status engram_enable_stage_timing(engram_ctx* ctx, int32_t enable);
 ENGRAM_API engram_status engram_stage_times(engram_ctx* ctx, float* ms);
 
+/* ---- allocation-free variant ------------------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers of
+ * this library that cannot allocate device memory.  A serving engine that
+ * reserves nearly all of HBM at start-up for its weights and KV cache and hands
+ * out every other byte through its own allocator, or a plugin running inside a
+ * host process that owns the GPU's memory budget, cannot let a library call
+ * cudaMalloc: the allocation may fail or synchronise at a point the caller does
+ * not control, and it escapes the caller's accounting.  engram_create() needs
+ * such allocations for its scratch; this call does not.
+ *
+ * engram_forward_noalloc() computes the same layer as engram_forward(), with
+ * the same kernels, for at most ENGRAM_NOALLOC_MAX_TOKENS tokens, without a
+ * context and without allocating: it calls no cudaMalloc, cudaFree or other
+ * allocating routine.  Its scratch (gathered rows, split-K partial sums,
+ * q_weight*k_weight, an error word) is one file-scope static __device__ array
+ * of ENGRAM_NOALLOC_SCRATCH_BYTES bytes; the CUDA driver places it in device
+ * memory when it loads this part of the library on a device, and every device
+ * that loads it keeps those bytes until the process exits.
+ *  - cfg and w are as for engram_create() (max_tokens and check_ids are
+ *    ignored); the weights are read on every call.  Shapes with
+ *    n_cols*head_dim > 6144 or dim*(hc_mult+1) > 25600 give ENGRAM_EUNSUPPORTED.
+ *  - B*T > ENGRAM_NOALLOC_MAX_TOKENS gives ENGRAM_EINVAL and queues nothing.
+ *  - The first call on each device looks up the device address of the scratch
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - Every call on a device shares the one scratch array, which keeps the last
+ *    call's contents; the call clears the part that must start at zero (the
+ *    error word) on `stream` before its kernels run.  Calls that overlap on the
+ *    GPU (other streams, other threads) race on the scratch: serialise them.
+ *  - Errors the device detects are not reported (there is no context to hold
+ *    them); every device wait stays bounded. */
+#define ENGRAM_NOALLOC_MAX_TOKENS 64
+#define ENGRAM_NOALLOC_SCRATCH_BYTES 20529408
+ENGRAM_API engram_status engram_forward_noalloc(const engram_config* cfg, const engram_weights* w,
+                                                const int64_t* hash_ids, const uint16_t* x,
+                                                const uint8_t* token_mask, uint16_t* out, int64_t B, int64_t T,
+                                                engram_stream_t stream);
+
 /* Static description of a status code. */
 ENGRAM_API const char* engram_status_string(engram_status s);
 
