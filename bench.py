@@ -259,10 +259,8 @@ def run_ours(args, w, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"engram_forward reported status {st} in warm-up")
 
-    # ---- device-timed steps (inputs resident in HBM)
-    layer.enable_stage_timing(True)
+    # ---- device-timed steps (inputs resident in HBM); one event pair per step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    stages = []
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -271,12 +269,21 @@ def run_ours(args, w, rank, world, local_rank):
         ev[i][0].record(stream)
         layer.forward(ids, x, mask, out=out)
         ev[i][1].record(stream)
-        stages.append(layer.stage_times())       # waits for this step's last event
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
+
+    # ---- per-kernel durations: the same steps again with an event between the
+    # kernels (events between kernels also stop them from overlapping, so these
+    # are each kernel's own duration, and they are not used for `value`)
+    layer.enable_stage_timing(True)
+    stages = []
+    for i in range(args.steps):
+        flush.zero_()
+        layer.forward(ids, x, mask, out=out)
+        stages.append(layer.stage_times())       # waits for this step's last event
     layer.enable_stage_timing(False)
 
     # keep the GPU busy a little longer so the clock sampler sees the load

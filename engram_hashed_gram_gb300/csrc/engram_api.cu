@@ -38,35 +38,6 @@ namespace {
 constexpr int kMaxSplits = 8;
 constexpr int64_t kSplitMaxTokens = 128;   // split-K only while one M tile covers the batch
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode;
-}
-
-// bf16 [rows, cols] row-major matrix, box = [box_rows, 64 columns], 128-byte swizzle
-bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Plan {
@@ -150,9 +121,6 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
   mark(c, 0, stream);
   if (launch_gather(g, c->num_sms, stream) != cudaSuccess) return ENGRAM_ECUDA;
   mark(c, 1, stream);
-  CUtensorMap tmA;
-  if (!make_tmap_bf16(&tmA, c->rows, static_cast<uint64_t>(M), static_cast<uint64_t>(c->K), kBM))
-    return ENGRAM_ECUDA;
   const Plan p = make_plan(c, M);
   GemmArgs a{};
   a.M = M;
@@ -168,7 +136,7 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
   a.kv = kv_out;
   a.part = c->part;
   a.err = c->err;
-  if (launch_gemm(tmA, c->tmW, a, p.ctas, stream) != cudaSuccess) return ENGRAM_ECUDA;
+  if (launch_gemm(c->rows, c->tmW, a, p.ctas, stream) != cudaSuccess) return ENGRAM_ECUDA;
   mark(c, 2, stream);
   *plan_out = p;
   return ENGRAM_OK;

@@ -7,13 +7,20 @@
 //   gate[s]   = sigmoid(copysign(sqrt(max(|dot|, clamp)), dot)), 0 if masked
 //   out[s, d] = bf16(h + gate[s] * value[d]); masked tokens copy x bit-for-bit.
 //
-// One CTA per token; thread t owns channels 8t..8t+7 of every stream, so all
-// loads are 16-byte vectors and the token's x, key and value are each read
-// once.  The three per-stream sums are reduced in a fixed order (warp
-// butterflies, then warps in index order): the result does not depend on
-// timing, and the path that reads fp32 split-K partials rounds kv to bf16
-// exactly as the separate reduction kernel does, so the fused layer and
-// lookup_project + gate_apply agree bit-for-bit.
+// A token is handled by a cluster of G CTAs (G = 4 for dim = 5120).  The
+// channels are cut into blocks of 256, one warp per block, so that lane l of a
+// warp owns channels 8l..8l+7 of its block in every stream: all loads are
+// 16-byte vectors and the token's x, key and value are each read once.
+//
+// Reduction order (fixed, and shared with any other kernel that forms these
+// sums): for each (stream, block), every lane accumulates its 8 channels in
+// order with fmaf starting from 0, the warp combines the 32 lane sums with an
+// xor butterfly (16, 8, 4, 2, 1), and the block sums are added in block order
+// starting from 0.  Each warp stores its block sums into the shared memory of
+// every CTA of the cluster (DSMEM); after one cluster barrier every CTA adds
+// them up locally.  The result does not depend on timing, and the
+// split-K path rounds kv to bf16 exactly as the separate reduction kernel does,
+// so engram_forward and lookup_project + gate_apply agree bit for bit.
 #include "common.cuh"
 #include "internal.cuh"
 
@@ -21,7 +28,9 @@ namespace engram {
 namespace {
 
 constexpr int kMaxHc = 4;
-constexpr int kGateMaxThreads = 640;   // dim / 8 for dim = 5120
+constexpr int kBlockCh = 256;                    // channels per reduction block (one warp)
+constexpr int kMaxBlocks = 5120 / kBlockCh;      // blocks per stream for dim = 5120
+constexpr int kGateMaxThreads = kMaxBlocks * 32;
 
 __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -49,71 +58,81 @@ __device__ __forceinline__ void load8_partials(const float* part, int splits, in
 
 template <bool FROM_PARTIALS>
 __global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const GateArgs a) {
-  __shared__ float red[32][3 * kMaxHc];
+  __shared__ float red[kMaxBlocks][3 * kMaxHc];   // every block's sums, pushed by the owning CTAs
+  __shared__ float tot[3 * kMaxHc];
   __shared__ float gate_s[kMaxHc];
 
-  grid_dependency_wait();
-  const int64_t m = blockIdx.x;
-  const int t = threadIdx.x;
+  const int G = a.cluster;
+  const uint32_t rank = G > 1 ? cluster_ctarank() : 0u;
+  const int64_t m = blockIdx.x / G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpc = blockDim.x >> 5;                 // blocks per CTA
+  const int nblocks = wpc * G;                     // blocks per stream
   const int D = a.dim;
   const int HC = a.hc;
   const int64_t N = static_cast<int64_t>(D) * (HC + 1);
-  const int d0 = 8 * t;
-  const bool active = d0 < D;
+  const int d0 = (static_cast<int>(rank) * wpc + warp) * kBlockCh + lane * 8;
   const uint16_t* xm = a.x + m * HC * D;
   uint16_t* om = a.out + m * HC * D;
 
+  // x and the mask are inputs of the call, written before the gather ran, so
+  // they may be read before the projection has finished
   if (a.mask != nullptr && a.mask[m] == 0) {
     // "pass through untouched": the streams are copied, the gate is 0
-    if (active && om != xm) {
+    grid_dependency_wait();
+    if (om != xm) {
       for (int s = 0; s < HC; ++s)
         *reinterpret_cast<uint4*>(om + s * D + d0) = __ldg(reinterpret_cast<const uint4*>(xm + s * D + d0));
     }
-    if (a.gates != nullptr && t < HC) a.gates[m * HC + t] = 0.0f;
+    if (a.gates != nullptr && rank == 0 && threadIdx.x < HC) a.gates[m * HC + threadIdx.x] = 0.0f;
+    grid_launch_dependents();
     return;
   }
 
   float h[kMaxHc][8];
+#pragma unroll
+  for (int s = 0; s < kMaxHc; ++s)
+    if (s < HC) unpack8(__ldg(reinterpret_cast<const uint4*>(xm + s * D + d0)), h[s]);
+
+  grid_dependency_wait();        // kv / the partial sums come from the projection
+  grid_launch_dependents();
+
   float v[8];
   float sums[3 * kMaxHc];
 #pragma unroll
   for (int i = 0; i < 3 * kMaxHc; ++i) sums[i] = 0.0f;
-
-  if (active) {
-    const int64_t split_stride = a.M * N;
+  const int64_t split_stride = a.M * N;
 #pragma unroll
-    for (int s = 0; s < kMaxHc; ++s) {
-      if (s < HC) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(xm + s * D + d0)), h[s]);
-        float k[8];
-        if (FROM_PARTIALS) {
-          load8_partials(a.part + m * N + s * D + d0, a.splits, split_stride, k);
-        } else {
-          unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + s * D + d0)), k);
-        }
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0));
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0) + 1);
-        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        float sh = 0.0f, sk = 0.0f, sd = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          sh = fmaf(h[s][j], h[s][j], sh);
-          sk = fmaf(k[j], k[j], sk);
-          sd = fmaf(h[s][j] * w[j], k[j], sd);
-        }
-        sums[3 * s + 0] = sh;
-        sums[3 * s + 1] = sk;
-        sums[3 * s + 2] = sd;
+  for (int s = 0; s < kMaxHc; ++s) {
+    if (s < HC) {
+      float k[8];
+      if (FROM_PARTIALS) {
+        load8_partials(a.part + m * N + s * D + d0, a.splits, split_stride, k);
+      } else {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + s * D + d0)), k);
       }
-    }
-    if (FROM_PARTIALS) {
-      load8_partials(a.part + m * N + static_cast<int64_t>(HC) * D + d0, a.splits, split_stride, v);
-    } else {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + static_cast<int64_t>(HC) * D + d0)), v);
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0));
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0) + 1);
+      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sh = fmaf(h[s][j], h[s][j], sh);
+        sk = fmaf(k[j], k[j], sk);
+        sd = fmaf(h[s][j] * w[j], k[j], sd);
+      }
+      sums[3 * s + 0] = sh;
+      sums[3 * s + 1] = sk;
+      sums[3 * s + 2] = sd;
     }
   }
+  if (FROM_PARTIALS) {
+    load8_partials(a.part + m * N + static_cast<int64_t>(HC) * D + d0, a.splits, split_stride, v);
+  } else {
+    unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + static_cast<int64_t>(HC) * D + d0)), v);
+  }
 
-  // block reduction in a fixed order
+  // one block sum per warp: xor butterfly 16, 8, 4, 2, 1
 #pragma unroll
   for (int i = 0; i < 3 * kMaxHc; ++i) {
     float x = sums[i];
@@ -121,49 +140,60 @@ __global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const Ga
     for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
     sums[i] = x;
   }
-  const int warp = t >> 5, lane = t & 31;
-  const int nwarps = (blockDim.x + 31) >> 5;
-  if (lane == 0) {
+  // every CTA of the cluster receives every block's sums: lane r of the warp
+  // stores them into CTA r (remote stores complete before the cluster barrier)
+  const int blk = static_cast<int>(rank) * wpc + warp;
+  if (G > 1) {
+    if (lane < G) {
 #pragma unroll
-    for (int i = 0; i < 3 * kMaxHc; ++i) red[warp][i] = sums[i];
+      for (int i = 0; i < 3 * kMaxHc; ++i) st_dsmem_f32(&red[blk][i], static_cast<uint32_t>(lane), sums[i]);
+    }
+    cluster_arrive();
+    cluster_wait();
+  } else {
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < 3 * kMaxHc; ++i) red[blk][i] = sums[i];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < 3 * HC) {            // one (stream, quantity) per thread, blocks in order
+    float acc = 0.0f;
+    for (int b = 0; b < nblocks; ++b) acc += red[b][threadIdx.x];
+    tot[threadIdx.x] = acc;
   }
   __syncthreads();
-  if (t < HC) {
-    float sh = 0.0f, sk = 0.0f, sd = 0.0f;
-    for (int w = 0; w < nwarps; ++w) {
-      sh += red[w][3 * t + 0];
-      sk += red[w][3 * t + 1];
-      sd += red[w][3 * t + 2];
-    }
+  if (threadIdx.x < HC) {
+    const int t = threadIdx.x;
     const float inv_d = 1.0f / static_cast<float>(D);
-    const float rstd = (1.0f / sqrtf(sh * inv_d + a.eps)) * (1.0f / sqrtf(sk * inv_d + a.eps));
-    const float dot = sd * rstd * a.inv_sqrt_dim;
+    const float rstd =
+        (1.0f / sqrtf(tot[3 * t] * inv_d + a.eps)) * (1.0f / sqrtf(tot[3 * t + 1] * inv_d + a.eps));
+    const float dot = tot[3 * t + 2] * rstd * a.inv_sqrt_dim;
     const float z = copysignf(sqrtf(fmaxf(fabsf(dot), a.clamp)), dot);
     const float g = 1.0f / (1.0f + expf(-z));
     gate_s[t] = g;
-    if (a.gates != nullptr) a.gates[m * HC + t] = g;
+    if (a.gates != nullptr && rank == 0) a.gates[m * HC + t] = g;
   }
   __syncthreads();
 
-  if (active) {
 #pragma unroll
-    for (int s = 0; s < kMaxHc; ++s) {
-      if (s < HC) {
-        const float g = gate_s[s];
-        uint4 o;
-        o.x = pack_bf16x2(fmaf(g, v[0], h[s][0]), fmaf(g, v[1], h[s][1]));
-        o.y = pack_bf16x2(fmaf(g, v[2], h[s][2]), fmaf(g, v[3], h[s][3]));
-        o.z = pack_bf16x2(fmaf(g, v[4], h[s][4]), fmaf(g, v[5], h[s][5]));
-        o.w = pack_bf16x2(fmaf(g, v[6], h[s][6]), fmaf(g, v[7], h[s][7]));
-        *reinterpret_cast<uint4*>(om + s * D + d0) = o;
-      }
+  for (int s = 0; s < kMaxHc; ++s) {
+    if (s < HC) {
+      const float g = gate_s[s];
+      uint4 o;
+      o.x = pack_bf16x2(fmaf(g, v[0], h[s][0]), fmaf(g, v[1], h[s][1]));
+      o.y = pack_bf16x2(fmaf(g, v[2], h[s][2]), fmaf(g, v[3], h[s][3]));
+      o.z = pack_bf16x2(fmaf(g, v[4], h[s][4]), fmaf(g, v[5], h[s][5]));
+      o.w = pack_bf16x2(fmaf(g, v[6], h[s][6]), fmaf(g, v[7], h[s][7]));
+      *reinterpret_cast<uint4*>(om + s * D + d0) = o;
     }
   }
-  grid_launch_dependents();
 }
 
 __global__ void reduce_partials_kernel(const float* __restrict__ part, int splits, int64_t MN,
                                        uint16_t* __restrict__ kv) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t n4 = MN >> 2;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -188,15 +218,19 @@ __global__ void weight_product_kernel(const uint16_t* __restrict__ q, const uint
 
 }  // namespace
 
-cudaError_t launch_gate(const GateArgs& a, cudaStream_t stream) {
-  if (a.M == 0) return cudaSuccess;
-  int threads = ((a.dim / 8) + 31) / 32 * 32;
-  if (a.part != nullptr) {
-    gate_residual_kernel<true><<<static_cast<unsigned>(a.M), threads, 0, stream>>>(a);
-  } else {
-    gate_residual_kernel<false><<<static_cast<unsigned>(a.M), threads, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
+int gate_cluster_size(int dim) {
+  const int nblocks = dim / kBlockCh;
+  return nblocks % 4 == 0 ? 4 : (nblocks % 2 == 0 ? 2 : 1);
+}
+
+cudaError_t launch_gate(const GateArgs& a_in, cudaStream_t stream) {
+  if (a_in.M == 0) return cudaSuccess;
+  GateArgs a = a_in;
+  a.cluster = gate_cluster_size(a.dim);
+  const unsigned threads = static_cast<unsigned>(a.dim / kBlockCh / a.cluster * 32);
+  const dim3 grid(static_cast<unsigned>(a.M * a.cluster));
+  if (a.part != nullptr) return launch_pdl(gate_residual_kernel<true>, grid, dim3(threads), 0, stream, a.cluster, a);
+  return launch_pdl(gate_residual_kernel<false>, grid, dim3(threads), 0, stream, a.cluster, a);
 }
 
 cudaError_t launch_reduce_partials(const float* part, int32_t splits, int64_t M, int32_t N, uint16_t* kv,
@@ -205,8 +239,8 @@ cudaError_t launch_reduce_partials(const float* part, int32_t splits, int64_t M,
   if (MN == 0) return cudaSuccess;
   int64_t blocks = (MN / 4 + 255) / 256;
   if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
-  reduce_partials_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, splits, MN, kv);
-  return cudaGetLastError();
+  return launch_pdl(reduce_partials_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, part,
+                    splits, MN, kv);
 }
 
 cudaError_t launch_weight_product(const uint16_t* q, const uint16_t* k, float* wprod, int64_t n,

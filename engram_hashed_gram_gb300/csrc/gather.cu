@@ -42,7 +42,8 @@ __device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& o0, uint
 
 template <int SCALE_FMT>
 __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
-  grid_dependency_wait();
+  grid_dependency_wait();        // the ids may come from the previous kernel
+  grid_launch_dependents();      // let the projection start its weight stream
   const int cpr = a.head_dim >> 4;              // 16-byte chunks per row
   const int nb = a.head_dim / a.scale_block;
   const int64_t total = a.rows_total * cpr;
@@ -73,7 +74,6 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
     dst[0] = lo;
     dst[1] = hi;
   }
-  grid_launch_dependents();
 }
 
 }  // namespace
@@ -85,12 +85,9 @@ cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream)
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // 8 resident CTAs of 256 per SM
   if (blocks > cap) blocks = cap;
-  if (a.scale_fmt == 0) {
-    gather_dequant_kernel<0><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
-  } else {
-    gather_dequant_kernel<1><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (a.scale_fmt == 0) return launch_pdl(gather_dequant_kernel<0>, grid, dim3(threads), 0, stream, 1, a);
+  return launch_pdl(gather_dequant_kernel<1>, grid, dim3(threads), 0, stream, 1, a);
 }
 
 }  // namespace engram

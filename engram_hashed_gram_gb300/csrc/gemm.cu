@@ -7,29 +7,43 @@
 // Design (sm_103a, one CTA per SM, persistent):
 //  * a work unit is a 128 x 256 output tile restricted to one K range
 //    (split-K); units are dealt round-robin to the CTAs;
-//  * warp 0 (one thread) streams A = E[128 rows, 64 k] and B = W[256 rows, 64 k]
-//    boxes with TMA (128-byte swizzle) into a 4-stage shared-memory ring;
+//  * warp 0 (one thread) streams A = E[A_ROWS rows, 64 k] and B = W[256 rows,
+//    64 k] boxes with TMA (128-byte swizzle) into a STAGES-deep shared-memory
+//    ring;
 //  * warp 1 (one thread) issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
 //    into one of two 256-column tensor-memory accumulators and commits each
 //    stage back to the producer;
 //  * warps 2-5 drain the other accumulator with tcgen05.ld and write either the
 //    bf16 kv (round to nearest even) or the fp32 partial sums of a K range;
 //  * no cluster, no multicast: the L2 serves the reuse of E and W across CTAs.
-// Rows of the last M tile past M read as zeros (TMA bounds fill) and are not
-// stored.
+// Variants: A_ROWS = 128 with 4 stages in general; for batches of at most 64
+// or 32 tokens the A box holds only 64 or 32 rows, and the shared memory that
+// frees goes to a deeper ring (5 or 6 stages), i.e. more of the weight stream
+// in flight per SM.  The MMA still reads 128 rows of A: rows past the box are
+// whatever the neighbouring shared memory holds, their accumulator rows are
+// never stored, and a row of D depends on its own row of A only.  Rows of the
+// last M tile past M read as zeros (TMA bounds fill) and are not stored.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.cuh"
 
 namespace engram {
 namespace {
 
-constexpr int kABytes = kBM * kBK * 2;        // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;        // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;        // two fp32 accumulators
-constexpr int kBarOffset = kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kBarOffset + kNumBars * 8 + 16;
+
+template <int A_ROWS, int STAGES>
+struct Cfg {
+  static constexpr int kABytes = A_ROWS * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOffset = STAGES * kStageBytes;
+  static constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
+  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kBarOffset + kNumBars * 8 + 16;
+  static_assert(kABytes % 1024 == 0, "A stages must stay 1024-byte aligned");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 
 __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& mt, int& nt, int& sp) {
   sp = static_cast<int>(u % a.splits);
@@ -48,9 +62,15 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned l
   atomicOr(err, kErrTimeout);
 }
 
+template <int A_ROWS, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
+  using C = Cfg<A_ROWS, STAGES>;
+  constexpr int kStages = STAGES;
+  constexpr int kABytes = C::kABytes;
+  constexpr int kStageBytes = C::kStageBytes;
+  constexpr int kBarOffset = C::kBarOffset;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
@@ -91,29 +111,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // E is written by the gather kernel queued before this one.
-  grid_dependency_wait();
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued[kStages] = {0, 0, 0, 0};
+      uint32_t issued[kStages] = {};
       bool ok = true;
+      // The weight does not depend on the kernel queued before this one (the
+      // gather): the first stages of the first unit get their weight tile while
+      // the gathered rows are still being written.
+      int pre = 0;
+      if (static_cast<int64_t>(blockIdx.x) < a.units) {
+        int mt, nt, sp;
+        unit_coords(a, blockIdx.x, mt, nt, sp);
+        pre = min(kStages, a.kb_per_split);
+        for (int i = 0; i < pre; ++i) {   // fresh ring: every stage is free
+          mbar_arrive_expect_tx(&full[i], kStageBytes);
+          tma_load_2d_hint(smB + i * kBBytes, &tmB, &full[i], (sp * a.kb_per_split + i) * kBK, nt * kBN, pol_w);
+        }
+      }
+      grid_dependency_wait();     // the gathered rows are written by the gather kernel
       for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        // the kernel queued after this one (the gate) may start arriving once
+        // every CTA has begun its last unit
+        if (u + gridDim.x >= a.units) grid_launch_dependents();
         int mt, nt, sp;
         unit_coords(a, u, mt, nt, sp);
         const int kb0 = sp * a.kb_per_split;
         for (int kb = 0; kb < a.kb_per_split; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
+          if (u == blockIdx.x && kb < pre) {
+            // weight tile already in flight on this stage: add the rows
+            tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], (kb0 + kb) * kBK, mt * kBM);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], (kb0 + kb) * kBK, mt * kBM);
+            tma_load_2d_hint(smB + stage * kBBytes, &tmB, &full[stage], (kb0 + kb) * kBK, nt * kBN, pol_w);
           }
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], (kb0 + kb) * kBK, mt * kBM);
-          tma_load_2d_hint(smB + stage * kBBytes, &tmB, &full[stage], (kb0 + kb) * kBK, nt * kBN, pol_w);
           ++issued[stage];
           if (++stage == kStages) {
             stage = 0;
@@ -131,6 +170,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    grid_dependency_wait();
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, kBN);
       int stage = 0;
@@ -139,6 +179,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        if (u + gridDim.x >= a.units) grid_launch_dependents();
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -177,11 +218,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    grid_dependency_wait();   // the outputs may still be read by an earlier kernel
     const int q = warp & 3;   // tensor-memory lane quarter this warp may read
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+      if (u + gridDim.x >= a.units) grid_launch_dependents();
       int mt, nt, sp;
       unit_coords(a, u, mt, nt, sp);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
@@ -233,20 +276,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-}  // namespace
-
-size_t gemm_smem_bytes() { return kSmemBytes; }
-
-cudaError_t gemm_prepare() {
-  return cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes));
+template <int A_ROWS, int STAGES>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(Cfg<A_ROWS, STAGES>::kSmemBytes));
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
+template <int A_ROWS, int STAGES>
+cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
+                           cudaStream_t stream) {
+  return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES>, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads),
+                    Cfg<A_ROWS, STAGES>::kSmemBytes, stream, 1, tmA, tmB, a);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int gemm_a_rows(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : kBM); }
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t gemm_prepare() {
+  cudaError_t e = set_smem_attr<128, 4>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 5>();
+  if (e == cudaSuccess) e = set_smem_attr<32, 6>();
+  return e;
+}
+
+cudaError_t launch_gemm(const uint16_t* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
                         cudaStream_t stream) {
   if (a.units == 0) return cudaSuccess;
-  wkv_gemm_kernel<<<ctas, kGemmThreads, kSmemBytes, stream>>>(tmA, tmB, a);
-  return cudaGetLastError();
+  const int ar = gemm_a_rows(a.M);
+  CUtensorMap tmA;
+  if (!make_tmap_bf16(&tmA, rows, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), static_cast<uint32_t>(ar)))
+    return cudaErrorInvalidValue;
+  if (ar == 32) return launch_variant<32, 6>(tmA, tmB, a, ctas, stream);
+  if (ar == 64) return launch_variant<64, 5>(tmA, tmB, a, ctas, stream);
+  return launch_variant<128, 4>(tmA, tmB, a, ctas, stream);
 }
 
 }  // namespace engram

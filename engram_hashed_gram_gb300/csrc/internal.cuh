@@ -9,6 +9,36 @@
 
 namespace engram {
 
+// Launches `kernel` on `stream` with programmatic dependent launch allowed (the
+// kernel may start while the previous kernel in the stream finishes; every
+// kernel here calls griddepcontrol.wait before it touches memory an earlier
+// kernel may still write, and triggers its dependents only after that wait)
+// and, when cluster_x > 1, in clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---- rows: gather + dequantise (steps a1-a3) ------------------------------
 struct GatherArgs {
   const int64_t* ids;       // [rows_total] global row ids (rows_total = M * n_cols)
@@ -29,7 +59,6 @@ cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream)
 constexpr int kBM = 128;     // tokens per tile (MMA M)
 constexpr int kBN = 256;     // kv columns per tile (MMA N)
 constexpr int kBK = 64;      // K elements per pipeline stage (one 128-byte swizzle row)
-constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;
 
 enum GemmOut : int32_t { kOutBf16 = 0, kOutPartial = 1 };
@@ -49,9 +78,14 @@ struct GemmArgs {
   float* part;           // kOutPartial: [splits, M, N]
   unsigned long long* err;
 };
-size_t gemm_smem_bytes();
 cudaError_t gemm_prepare();   // per-device one-time kernel attributes
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
+// Rows of the A (gathered rows) box the projection uses for a batch of M tokens.
+int gemm_a_rows(int64_t M);
+// bf16 [rows, cols] row-major matrix, box = [box_rows, 64 columns], 128-byte swizzle.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// rows: the gathered rows [M, K] (its tensor map is built here, to match the
+// kernel variant); tmB: the weight's map, box [256 rows, 64 columns].
+cudaError_t launch_gemm(const uint16_t* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
                         cudaStream_t stream);
 
 // ---- gate and residual (steps a5-a8) ---------------------------------------
@@ -70,6 +104,7 @@ struct GateArgs {
   float eps;
   float clamp;
   float inv_sqrt_dim;
+  int32_t cluster;        // CTAs per token (set by launch_gate)
 };
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t stream);
 

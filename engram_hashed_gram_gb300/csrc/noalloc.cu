@@ -61,32 +61,6 @@ cudaError_t scratch_address(int dev, unsigned char** out) {
   return cudaSuccess;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-bool tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
@@ -172,10 +146,8 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   g.err = err;
   if (launch_gather(g, sms, s) != cudaSuccess) return ENGRAM_ECUDA;
 
-  CUtensorMap tmA, tmB;
-  if (!tmap_bf16(&tmA, rows, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kBM) ||
-      !tmap_bf16(&tmB, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN))
-    return ENGRAM_ECUDA;
+  CUtensorMap tmB;
+  if (!make_tmap_bf16(&tmB, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN)) return ENGRAM_ECUDA;
   GemmArgs a{};
   a.M = M;
   a.N = static_cast<int32_t>(N);
@@ -192,7 +164,7 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   a.err = err;
   if (gemm_prepare() != cudaSuccess) return ENGRAM_ECUDA;
   const int ctas = static_cast<int>(a.units < sms ? a.units : sms);
-  if (launch_gemm(tmA, tmB, a, ctas, s) != cudaSuccess) return ENGRAM_ECUDA;
+  if (launch_gemm(rows, tmB, a, ctas, s) != cudaSuccess) return ENGRAM_ECUDA;
 
   GateArgs ga{};
   ga.x = x;
