@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "Engram layer tokens/s (prefill, decode); gather HBM GB/s; % of roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "decode_64x1"
+ARGS = None
 FLUSH_BYTES = 256 << 20
 
 
@@ -224,7 +225,7 @@ def config_of(w):
     return {"workload": w.name, "B": w.B, "T": w.T, "tokens": w.M, "dim": w.dim, "hc_mult": w.hc_mult,
             "n_cols": w.n_cols, "head_dim": w.head_dim, "table_rows": w.num_rows(),
             "table_gb": round(w.num_rows() * w.head_dim / 1e9, 2), "hash_ids": w.ids, "mask": w.mask,
-            "prime_base": w.prime_base, "wkv": "bf16 [25600, 6144]",
+            "prime_base": w.prime_base, "wkv": "bf16 [25600, 6144]", "fuse_gate": bool(getattr(ARGS, "fuse_gate", False)),
             "l2": "flushed between timed steps (256 MB write)"}
 
 
@@ -244,7 +245,7 @@ def run_ours(args, w, rank, world, local_rank):
     inp = synth.make_inputs(w)
     table, scale = SD.make_table(w, device=dev)
     d = SD.upload_inputs(inp, device=dev)
-    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps)
+    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps, fuse_gate=args.fuse_gate)
     ids, x, mask = d["hash_ids"], d["x"], d["mask"]
     out = torch.empty_like(x)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -401,11 +402,15 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fuse-gate", action="store_true",
+                    help="form the gate in the projection's epilogue (engram_config.fuse_gate)")
     ap.add_argument("--prime-base", type=int, default=None,
                     help="profiling only: build the table from the 24 primes above this base instead of the "
                          "workload's (the projection and gate kernels do the same work; the gather reads a "
                          "smaller table)")
     args = ap.parse_args()
+    global ARGS
+    ARGS = args
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 

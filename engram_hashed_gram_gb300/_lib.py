@@ -41,6 +41,7 @@ class EngramConfig(ctypes.Structure):
         ("clamp", c_float),
         ("max_tokens", c_int32),
         ("check_ids", c_int32),
+        ("fuse_gate", c_int32),
     ]
 
 

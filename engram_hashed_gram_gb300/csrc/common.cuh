@@ -245,4 +245,37 @@ __device__ __forceinline__ float round_bf16(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// The gate of one (token, stream) from its three sums over the channels
+// (atlas.klimoza.dev "deepseek-v4.1 / engram-second", `Engram.forward`):
+// rstd = 1/sqrt(sh/D + eps) * 1/sqrt(sk/D + eps), dot = sd * rstd * D^-0.5,
+// gate = sigmoid(copysign(sqrt(max(|dot|, clamp)), dot)).  Written with
+// explicit roundings (no contraction) so that every kernel that forms it gets
+// the same bits.
+__device__ __forceinline__ float engram_gate(float sh, float sk, float sd, int D, float eps, float clamp,
+                                             float inv_sqrt_dim) {
+  const float inv_d = 1.0f / static_cast<float>(D);
+  const float rh = 1.0f / sqrtf(__fadd_rn(__fmul_rn(sh, inv_d), eps));
+  const float rk = 1.0f / sqrtf(__fadd_rn(__fmul_rn(sk, inv_d), eps));
+  const float dot = __fmul_rn(__fmul_rn(sd, __fmul_rn(rh, rk)), inv_sqrt_dim);
+  const float z = copysignf(sqrtf(fmaxf(fabsf(dot), clamp)), dot);
+  return 1.0f / __fadd_rn(1.0f, expf(-z));
+}
+
+// Acquire load / release add on a global counter shared by the CTAs of a grid.
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t atom_acq_rel_add_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 }  // namespace engram

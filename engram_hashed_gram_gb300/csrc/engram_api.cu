@@ -28,6 +28,9 @@ struct engram_ctx {
   float* part;                // [kMaxSplits, part_tokens, N] fp32
   int64_t part_tokens;
   unsigned long long* err;    // device [2]
+  float* gsum;                // [max_tokens, hc, dim/256, 4] fused-epilogue block sums
+  float* gates;               // [max_tokens, 4] fused-epilogue gates
+  uint32_t* counters;         // [ceil(max_tokens/128), 8] fused-epilogue counters and flags
   CUtensorMap tmW;
   cudaEvent_t ev[4];          // stage timing (null unless enabled)
   bool timing;
@@ -68,6 +71,14 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
       }
     }
   }
+  // tuning override for measurements: ENGRAM_SPLITS=<s> forces a split-K factor
+  static const int forced = [] {
+    const char* e = std::getenv("ENGRAM_SPLITS");
+    return e != nullptr ? std::atoi(e) : 0;
+  }();
+  if (forced >= 1 && forced <= kMaxSplits && kbt % forced == 0 &&
+      (forced == 1 || (M <= kSplitMaxTokens && M <= c->part_tokens)))
+    best = forced;
   p.splits = best;
   p.units = tiles * best;
   p.ctas = static_cast<int32_t>(p.units < c->num_sms ? p.units : c->num_sms);
@@ -112,16 +123,32 @@ GatherArgs gather_args(const engram_ctx* c, const int64_t* ids, uint16_t* out, i
   return g;
 }
 
-// gathered rows -> projection; writes bf16 kv to kv_out when splits == 1, the
-// fp32 partials to the context otherwise.  Returns the plan used.
-engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint16_t* kv_out, Plan* plan_out,
-                             cudaStream_t stream) {
+// The hidden-state side of engram_forward: with it, a plan without split-K runs
+// the gate and the residual add in the projection's epilogue.
+struct FusedIO {
+  const uint16_t* x;
+  const uint8_t* mask;
+  uint16_t* out;
+};
+
+bool fuses(const Plan& p, int64_t M) { return p.splits == 1 && gemm_can_fuse(M); }
+
+// gathered rows -> projection.  With `fused` and a fusable plan it writes the
+// layer's output; otherwise bf16 kv to kv_out when splits == 1 and the fp32
+// partial sums to the context when splits > 1.
+engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint16_t* kv_out, const FusedIO* fused,
+                             Plan* plan_out, cudaStream_t stream) {
   if (cudaSetDevice(c->device) != cudaSuccess) return ENGRAM_ECUDA;
+  const Plan p = make_plan(c, M);
+  const bool fuse = fused != nullptr && c->cfg.fuse_gate && fuses(p, M);
   GatherArgs g = gather_args(c, ids, c->rows, M);
+  if (fuse) {
+    g.zero = c->counters;
+    g.n_zero = p.m_tiles * 8;
+  }
   mark(c, 0, stream);
   if (launch_gather(g, c->num_sms, stream) != cudaSuccess) return ENGRAM_ECUDA;
   mark(c, 1, stream);
-  const Plan p = make_plan(c, M);
   GemmArgs a{};
   a.M = M;
   a.N = c->N;
@@ -136,6 +163,22 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
   a.kv = kv_out;
   a.part = c->part;
   a.err = c->err;
+  if (fuse) {
+    a.out_mode = kOutFused;
+    a.x = fused->x;
+    a.mask = fused->mask;
+    a.wprod = c->wprod;
+    a.out = fused->out;
+    a.gsum = c->gsum;
+    a.counters = c->counters;
+    a.gates = c->gates;
+    a.key_n_tiles = c->cfg.hc_mult * c->cfg.dim / kBN;
+    a.dim = c->cfg.dim;
+    a.hc = c->cfg.hc_mult;
+    a.eps = c->cfg.eps;
+    a.clamp = c->cfg.clamp;
+    a.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c->cfg.dim)));
+  }
   if (launch_gemm(c->rows, c->tmW, a, p.ctas, stream) != cudaSuccess) return ENGRAM_ECUDA;
   mark(c, 2, stream);
   *plan_out = p;
@@ -167,6 +210,9 @@ void free_ctx(engram_ctx* c) {
   cudaFree(c->kv);
   cudaFree(c->part);
   cudaFree(c->err);
+  cudaFree(c->gsum);
+  cudaFree(c->counters);
+  cudaFree(c->gates);
   delete c;
 }
 
@@ -235,7 +281,12 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
             cudaMalloc(&ctx->rows, static_cast<size_t>(mt) * K * 2) == cudaSuccess &&
             cudaMalloc(&ctx->kv, static_cast<size_t>(mt) * N * 2) == cudaSuccess &&
             cudaMalloc(&ctx->part, static_cast<size_t>(kMaxSplits) * ctx->part_tokens * N * 4) == cudaSuccess &&
-            cudaMalloc(&ctx->err, 2 * sizeof(unsigned long long)) == cudaSuccess;
+            cudaMalloc(&ctx->err, 2 * sizeof(unsigned long long)) == cudaSuccess &&
+            cudaMalloc(&ctx->gsum, static_cast<size_t>(mt) * c.hc_mult * (c.dim / kBN) * 4 * sizeof(float)) ==
+                cudaSuccess &&
+            cudaMalloc(&ctx->counters, static_cast<size_t>((mt + kBM - 1) / kBM) * 8 * sizeof(uint32_t)) ==
+                cudaSuccess &&
+            cudaMalloc(&ctx->gates, static_cast<size_t>(mt) * 4 * sizeof(float)) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_ctx(ctx);
@@ -275,8 +326,13 @@ engram_status engram_forward(engram_ctx* ctx, const int64_t* hash_ids, const uin
   if (!aligned(hash_ids, 8) || !aligned(x, 16) || !aligned(out, 16)) return ENGRAM_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Plan p{};
-  st = run_projection(ctx, hash_ids, M, ctx->kv, &p, s);
+  const FusedIO io{x, token_mask, out};
+  st = run_projection(ctx, hash_ids, M, ctx->kv, &io, &p, s);
   if (st != ENGRAM_OK) return st;
+  if (ctx->cfg.fuse_gate && fuses(p, M)) {   // the projection's epilogue applied the gate
+    mark(ctx, 3, s);
+    return ENGRAM_OK;
+  }
   GateArgs g = gate_args(ctx, x, token_mask, out, nullptr, M);
   if (p.splits == 1) {
     g.kv = ctx->kv;
@@ -299,7 +355,7 @@ engram_status engram_lookup_project(engram_ctx* ctx, const int64_t* hash_ids, ui
   if (hash_ids == nullptr || kv == nullptr || !aligned(hash_ids, 8) || !aligned(kv, 16)) return ENGRAM_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Plan p{};
-  st = run_projection(ctx, hash_ids, M, kv, &p, s);
+  st = run_projection(ctx, hash_ids, M, kv, nullptr, &p, s);
   if (st != ENGRAM_OK) return st;
   if (p.splits > 1) st = cuda_status(launch_reduce_partials(ctx->part, p.splits, M, ctx->N, kv, ctx->num_sms, s));
   mark(ctx, 3, s);

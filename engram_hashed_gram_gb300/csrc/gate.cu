@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const Ga
       for (int j = 0; j < 8; ++j) {
         sh = fmaf(h[s][j], h[s][j], sh);
         sk = fmaf(k[j], k[j], sk);
-        sd = fmaf(h[s][j] * w[j], k[j], sd);
+        sd = fmaf(__fmul_rn(h[s][j], w[j]), k[j], sd);
       }
       sums[3 * s + 0] = sh;
       sums[3 * s + 1] = sk;
@@ -165,12 +165,7 @@ __global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const Ga
   __syncthreads();
   if (threadIdx.x < HC) {
     const int t = threadIdx.x;
-    const float inv_d = 1.0f / static_cast<float>(D);
-    const float rstd =
-        (1.0f / sqrtf(tot[3 * t] * inv_d + a.eps)) * (1.0f / sqrtf(tot[3 * t + 1] * inv_d + a.eps));
-    const float dot = tot[3 * t + 2] * rstd * a.inv_sqrt_dim;
-    const float z = copysignf(sqrtf(fmaxf(fabsf(dot), a.clamp)), dot);
-    const float g = 1.0f / (1.0f + expf(-z));
+    const float g = engram_gate(tot[3 * t], tot[3 * t + 1], tot[3 * t + 2], D, a.eps, a.clamp, a.inv_sqrt_dim);
     gate_s[t] = g;
     if (a.gates != nullptr && rank == 0) a.gates[m * HC + t] = g;
   }

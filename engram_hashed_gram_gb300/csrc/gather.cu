@@ -44,6 +44,9 @@ template <int SCALE_FMT>
 __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
   grid_dependency_wait();        // the ids may come from the previous kernel
   grid_launch_dependents();      // let the projection start its weight stream
+  if (a.zero != nullptr) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero; i += gridDim.x * blockDim.x) a.zero[i] = 0u;
+  }
   const int cpr = a.head_dim >> 4;              // 16-byte chunks per row
   const int nb = a.head_dim / a.scale_block;
   const int64_t total = a.rows_total * cpr;

@@ -34,32 +34,319 @@ namespace {
 constexpr int kBBytes = kBN * kBK * 2;        // 32 KB
 constexpr uint32_t kTmemCols = 2 * kBN;        // two fp32 accumulators
 
+constexpr int kMaxStreams = 4;                 // hc_mult
+constexpr int kMaxBlocks = 5120 / kBN;         // 256-channel blocks per stream (dim <= 5120)
+
+// Per epilogue warp, fused mode only: 32 rows x 32 bf16 of a value tile
+// (pitch 80 bytes: conflict-free 16-byte accesses), the rows' gates and
+// pass-through flags.  Key tiles use its first 1 KB for the tile's q*k.
+constexpr int kEpiPitch = 80;
+constexpr int kEpiGates = 32 * kEpiPitch;            // float [32][4]
+constexpr int kEpiFlags = kEpiGates + 32 * 16;       // int [32]
+constexpr int kEpiWarpBytes = kEpiFlags + 32 * 4;    // 3,200
+
 template <int A_ROWS, int STAGES>
 struct Cfg {
   static constexpr int kABytes = A_ROWS * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
-  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kBarOffset + kNumBars * 8 + 16;
+  static constexpr int kEpiOffset = kBarOffset + 256;              // fused-mode staging, after the barriers
+  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kEpiOffset;
+  static constexpr size_t kSmemFused = kSmemBytes + 4 * kEpiWarpBytes;
+  static constexpr bool kCanFuse = kSmemFused <= 232448;
+  static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
   static_assert(kABytes % 1024 == 0, "A stages must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-__device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& mt, int& nt, int& sp) {
-  sp = static_cast<int>(u % a.splits);
-  const int64_t t = u / a.splits;
-  const int64_t group_tiles = static_cast<int64_t>(a.group_m) * a.n_tiles;
+// Tile t of an m_tiles x n_count grid, rasterised in groups of group_m M tiles
+// (M fastest inside a group) so that tiles running at the same time share
+// their A and B tiles in L2.
+__device__ __forceinline__ void raster(const GemmArgs& a, int64_t t, int n_count, int& mt, int& ntl) {
+  const int64_t group_tiles = static_cast<int64_t>(a.group_m) * n_count;
   const int64_t g = t / group_tiles;
   const int64_t r = t - g * group_tiles;
   const int gm0 = static_cast<int>(g) * a.group_m;
   const int gm = min(a.group_m, a.m_tiles - gm0);
-  nt = static_cast<int>(r / gm);
+  ntl = static_cast<int>(r / gm);
   mt = gm0 + static_cast<int>(r % gm);
+}
+
+// Unit u -> (M tile, N tile, K split).  In the fused mode every key tile comes
+// before every value tile: a value tile waits only for units with smaller
+// indices, and by the time any CTA reaches the value tiles nearly all key
+// tiles are done.
+__device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& mt, int& nt, int& sp) {
+  sp = static_cast<int>(u % a.splits);
+  const int64_t t = u / a.splits;
+  if (a.out_mode == kOutFused) {
+    const int64_t key_units = static_cast<int64_t>(a.m_tiles) * a.key_n_tiles;
+    if (t < key_units) {
+      raster(a, t, a.key_n_tiles, mt, nt);
+    } else {
+      raster(a, t - key_units, a.n_tiles - a.key_n_tiles, mt, nt);
+      nt += a.key_n_tiles;
+    }
+    return;
+  }
+  raster(a, t, a.n_tiles, mt, nt);
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned long long* err) {
   *abort_flag = 1;
   atomicOr(err, kErrTimeout);
+}
+
+// kv (bf16) or the fp32 split-K partial sums of row m, columns [nt*256, nt*256 + 256).
+__device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m, int nt, int sp) {
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+    tmem_ld_wait();
+    if (m < a.M) {
+      const int n0 = nt * kBN + c * 32;
+      if (a.out_mode == kOutBf16) {
+        uint4* dst = reinterpret_cast<uint4*>(a.kv + m * a.N + n0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dst[j] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                              pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                              pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                              pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+        }
+      } else {
+        float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(sp) * a.M + m) * a.N + n0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          dst[j] = make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- fused epilogue
+// The fused epilogue forms the gate kernel's sums in the gate kernel's order
+// (gate.cu): a 256-channel block of one stream is 32 groups of 8 channels; a
+// group's sum is an fmaf chain over its channels from 0; the 32 group sums
+// combine as an xor butterfly over 32 lanes would (x_l + x_{l+16} for l < 16,
+// then + x_{l+8} for l < 8, ... -- IEEE addition is commutative, so every lane
+// of the butterfly holds these bits); blocks are added in block order from 0.
+// With the same bf16 kv values (this kernel's accumulators rounded as
+// lookup_project rounds them) the gates and outputs equal those of
+// lookup_project followed by gate_apply, bit for bit.
+
+__device__ __forceinline__ void unpack8_bf16(uint4 v, float* f) {
+  f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// Key tile: row m's block sums of stream s, channels [d0, d0 + 256).  The warp
+// first copies the tile's 256 weight products (the same for every row) to its
+// shared memory; row m's hidden state is loaded one 32-channel chunk ahead.
+__device__ __forceinline__ void fused_key_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m, int n0, int lane,
+                                                   float* wsm) {
+  const int s = n0 / a.dim;
+  const int d0 = n0 - s * a.dim;
+  const bool active = m < a.M && (a.mask == nullptr || a.mask[m] != 0);
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (m * a.hc + s) * a.dim + d0);
+  {
+    const float4* wg = reinterpret_cast<const float4*>(a.wprod + static_cast<int64_t>(s) * a.dim + d0) + 2 * lane;
+    reinterpret_cast<float4*>(wsm)[2 * lane] = __ldg(wg);
+    reinterpret_cast<float4*>(wsm)[2 * lane + 1] = __ldg(wg + 1);
+    __syncwarp();
+  }
+  float th[16], tk[16], td[16];   // the butterfly after its first step
+  uint4 hcur[4], hnext[4];
+  if (active) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) hcur[g] = __ldg(xr + g);
+  }
+#pragma unroll
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+    if (active && c + 1 < kBN / 32) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) hnext[g] = __ldg(xr + 4 * (c + 1) + g);
+    }
+    tmem_ld_wait();
+    if (active) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int l = 4 * c + g;                     // group index in the block
+        float h[8];
+        unpack8_bf16(hcur[g], h);
+        const float4 w0 = reinterpret_cast<const float4*>(wsm)[2 * l];
+        const float4 w1 = reinterpret_cast<const float4*>(wsm)[2 * l + 1];
+        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float k = round_bf16(__uint_as_float(r[8 * g + j]));
+          sh = fmaf(h[j], h[j], sh);
+          sk = fmaf(k, k, sk);
+          sd = fmaf(__fmul_rn(h[j], w[j]), k, sd);
+        }
+        if (l < 16) {
+          th[l] = sh; tk[l] = sk; td[l] = sd;
+        } else {                                     // butterfly step 16
+          th[l - 16] = th[l - 16] + sh; tk[l - 16] = tk[l - 16] + sk; td[l - 16] = td[l - 16] + sd;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) hcur[g] = hnext[g];
+    }
+  }
+  __syncwarp();                                      // wsm is rewritten by the next tile
+  if (active) {
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+#pragma unroll
+      for (int l = 0; l < off; ++l) {
+        th[l] = th[l] + th[l + off]; tk[l] = tk[l] + tk[l + off]; td[l] = td[l] + td[l + off];
+      }
+    }
+    const int nblk = a.dim / kBN;
+    reinterpret_cast<float4*>(a.gsum)[(m * a.hc + s) * nblk + d0 / kBN] = make_float4(th[0], tk[0], td[0], 0.0f);
+  }
+}
+
+// Called by every key-tile warp after its block sums are written.  The last
+// warp to arrive for an (M tile, lane quarter) -- the counter's old value tells
+// it -- forms the gates of the quarter's 32 rows from all block sums, stores
+// them and raises the quarter's ready flag, so that value tiles read one float4
+// per row instead of summing the blocks themselves.
+__device__ __forceinline__ void fused_key_publish(const GemmArgs& a, int64_t m, int mt, int q, int lane) {
+  __syncwarp();
+  uint32_t old = 0;
+  if (lane == 0) old = atom_acq_rel_add_u32(a.counters + mt * 8 + q, 1u);
+  old = __shfl_sync(0xFFFFFFFFu, old, 0);
+  if (old + 1 != static_cast<uint32_t>(a.key_n_tiles)) return;
+  __threadfence();                                   // every block sum of these rows is visible now
+  if (m < a.M) {
+    float g[kMaxStreams] = {};
+    if (a.mask == nullptr || a.mask[m] != 0) {
+      const int nblk = a.dim / kBN;
+#pragma unroll
+      for (int s = 0; s < kMaxStreams; ++s) {
+        if (s >= a.hc) break;
+        const float4* p = reinterpret_cast<const float4*>(a.gsum) + (m * a.hc + s) * nblk;
+        float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+#pragma unroll
+        for (int b0 = 0; b0 < kMaxBlocks; b0 += kMaxBlocks / 2) {   // two batches of loads in flight
+          float4 blk[kMaxBlocks / 2];
+#pragma unroll
+          for (int b = 0; b < kMaxBlocks / 2; ++b)
+            if (b0 + b < nblk) blk[b] = __ldcg(p + b0 + b);
+#pragma unroll
+          for (int b = 0; b < kMaxBlocks / 2; ++b) {  // block order
+            if (b0 + b < nblk) {
+              sh += blk[b].x;
+              sk += blk[b].y;
+              sd += blk[b].z;
+            }
+          }
+        }
+        g[s] = engram_gate(sh, sk, sd, a.dim, a.eps, a.clamp, a.inv_sqrt_dim);
+      }
+    }
+    reinterpret_cast<float4*>(a.gates)[m] = make_float4(g[0], g[1], g[2], g[3]);
+  }
+  __syncwarp();
+  if (lane == 0) red_release_add_u32(a.counters + mt * 8 + 4 + q, 1u);
+}
+
+// Value tile: once the gates of the warp's 32 rows are ready, out = h + gate *
+// value for channels [d0, d0 + 256) of every stream.  Each 32-channel chunk of
+// the value passes through the warp's shared-memory tile so that 4 lanes cover
+// one row's 64 contiguous bytes of x and out (8 rows per warp instruction
+// instead of 32).  Returns false if the wait ran out.
+__device__ __forceinline__ bool fused_value_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m, int mt, int q,
+                                                     int n0, int lane, volatile int* abort_flag, uint8_t* epi) {
+  const int d0 = n0 - a.hc * a.dim;
+  bool ok = true;
+  if (lane == 0) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (ld_acquire_u32(a.counters + mt * 8 + 4 + q) == 0u) {
+      if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  if (!ok) return false;
+  __threadfence();
+  float* gsm = reinterpret_cast<float*>(epi + kEpiGates);
+  int* fsm = reinterpret_cast<int*>(epi + kEpiFlags);
+  {
+    const bool active = m < a.M;
+    const bool pass = active && a.mask != nullptr && a.mask[m] == 0;
+    reinterpret_cast<float4*>(gsm)[lane] =
+        active && !pass ? __ldcg(reinterpret_cast<const float4*>(a.gates) + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+    fsm[lane] = active ? (pass ? 2 : 1) : 0;
+  }
+  __syncwarp();
+  const int64_t m0 = m - lane;                       // the warp's first row
+  const int cg = (lane & 3) * 8;                     // this lane's 8 channels of a chunk
+  int flag[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) flag[i] = fsm[(lane >> 2) + 8 * i];
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+    tmem_ld_wait();
+    uint4* vrow = reinterpret_cast<uint4*>(epi + lane * kEpiPitch);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)                      // kv rounded to bf16, as the projection returns it
+      vrow[j] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                           pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                           pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                           pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+    __syncwarp();
+    uint4 hb[4][kMaxStreams];                        // all of the chunk's x loads in flight together
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4* xr =
+          reinterpret_cast<const uint4*>(a.x + ((m0 + (lane >> 2) + 8 * i) * a.hc) * a.dim + d0 + c * 32 + cg);
+#pragma unroll
+      for (int s = 0; s < kMaxStreams; ++s)
+        if (flag[i] != 0 && s < a.hc) hb[i][s] = __ldg(xr + s * (a.dim / 8));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (flag[i] == 0) continue;
+      const int rl = (lane >> 2) + 8 * i;
+      const int64_t mr = m0 + rl;
+      float v[8];
+      unpack8_bf16(*reinterpret_cast<const uint4*>(epi + rl * kEpiPitch + cg * 2), v);
+#pragma unroll
+      for (int s = 0; s < kMaxStreams; ++s) {
+        if (s >= a.hc) break;
+        uint4 o = hb[i][s];
+        if (flag[i] == 1) {
+          const float gs = gsm[4 * rl + s];
+          float h[8];
+          unpack8_bf16(hb[i][s], h);
+          o.x = pack_bf16x2(fmaf(gs, v[0], h[0]), fmaf(gs, v[1], h[1]));
+          o.y = pack_bf16x2(fmaf(gs, v[2], h[2]), fmaf(gs, v[3], h[3]));
+          o.z = pack_bf16x2(fmaf(gs, v[4], h[4]), fmaf(gs, v[5], h[5]));
+          o.w = pack_bf16x2(fmaf(gs, v[6], h[6]), fmaf(gs, v[7], h[7]));
+        }
+        *reinterpret_cast<uint4*>(a.out + (mr * a.hc + s) * a.dim + d0 + c * 32 + cg) = o;
+      }
+    }
+    __syncwarp();                                    // the tile is rewritten by the next chunk
+  }
+  return true;
 }
 
 template <int A_ROWS, int STAGES>
@@ -220,6 +507,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ epilogue
     grid_dependency_wait();   // the outputs may still be read by an earlier kernel
     const int q = warp & 3;   // tensor-memory lane quarter this warp may read
+    uint8_t* epi = smem + C::kEpiOffset + (warp - 2) * kEpiWarpBytes;   // fused-mode staging of this warp
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -234,31 +522,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-#pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
-        tmem_ld_wait();
-        if (m < a.M) {
-          const int n0 = nt * kBN + c * 32;
-          if (a.out_mode == kOutBf16) {
-            uint4* dst = reinterpret_cast<uint4*>(a.kv + m * a.N + n0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              dst[j] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
-                                  pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
-                                  pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
-                                  pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(sp) * a.M + m) * a.N + n0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              dst[j] = make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
-                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            }
-          }
-        }
+      if (a.out_mode != kOutFused) {
+        plain_epilogue(a, t_row, m, nt, sp);
+      } else if (nt < a.key_n_tiles) {
+        fused_key_epilogue(a, t_row, m, nt * kBN, lane, reinterpret_cast<float*>(epi));
+        fused_key_publish(a, m, mt, q, lane);
+      } else if (!fused_value_epilogue(a, t_row, m, mt, q, nt * kBN, lane, abort_flag, epi)) {
+        ok = false;
+        break;
       }
       tc_fence_before();
       __syncwarp();
@@ -278,15 +549,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <int A_ROWS, int STAGES>
 cudaError_t set_smem_attr() {
+  using C = Cfg<A_ROWS, STAGES>;
   return cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(Cfg<A_ROWS, STAGES>::kSmemBytes));
+                              static_cast<int>(C::kCanFuse ? C::kSmemFused : C::kSmemBytes));
 }
 
 template <int A_ROWS, int STAGES>
 cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
                            cudaStream_t stream) {
+  using C = Cfg<A_ROWS, STAGES>;
+  const bool fused = a.out_mode == kOutFused;
+  if (fused && !C::kCanFuse) return cudaErrorInvalidConfiguration;
   return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES>, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads),
-                    Cfg<A_ROWS, STAGES>::kSmemBytes, stream, 1, tmA, tmB, a);
+                    fused ? C::kSmemFused : C::kSmemBytes, stream, 1, tmA, tmB, a);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -306,6 +581,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 int gemm_a_rows(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : kBM); }
+
+bool gemm_can_fuse(int64_t M) {
+  const int ar = gemm_a_rows(M);
+  return ar == 32 ? Cfg<32, 6>::kCanFuse : (ar == 64 ? Cfg<64, 5>::kCanFuse : Cfg<128, 4>::kCanFuse);
+}
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto enc = encode_fn();

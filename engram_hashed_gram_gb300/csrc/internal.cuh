@@ -52,6 +52,8 @@ struct GatherArgs {
   int32_t scale_fmt;
   int32_t check_ids;
   unsigned long long* err;  // [0]: flags, [1]: count of ids out of range
+  uint32_t* zero;           // words the kernel that follows needs cleared (may be null)
+  int32_t n_zero;
 };
 cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
 
@@ -61,7 +63,7 @@ constexpr int kBN = 256;     // kv columns per tile (MMA N)
 constexpr int kBK = 64;      // K elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kGemmThreads = 192;
 
-enum GemmOut : int32_t { kOutBf16 = 0, kOutPartial = 1 };
+enum GemmOut : int32_t { kOutBf16 = 0, kOutPartial = 1, kOutFused = 2 };
 
 struct GemmArgs {
   int64_t M;
@@ -77,10 +79,26 @@ struct GemmArgs {
   uint16_t* kv;          // kOutBf16: [M, N]
   float* part;           // kOutPartial: [splits, M, N]
   unsigned long long* err;
+  // kOutFused (splits == 1): the gate and the residual add run in the epilogue
+  const uint16_t* x;     // [M, hc, dim]
+  const uint8_t* mask;   // [M] or nullptr
+  const float* wprod;    // [hc, dim]
+  uint16_t* out;         // [M, hc, dim]
+  float* gsum;           // [M, hc, dim/256, 4]: block sums of h^2, key^2, h*w*key
+  float* gates;          // [M, 4] the gates of every row, formed by the last key warp of its quarter
+  uint32_t* counters;    // [m_tiles, 8]: key tiles done per lane quarter, then gates-ready flags; zeroed by the gather
+  int32_t key_n_tiles;   // n-tiles of the keys (hc*dim/256); every key unit precedes every value unit
+  int32_t dim;
+  int32_t hc;
+  float eps;
+  float clamp;
+  float inv_sqrt_dim;
 };
 cudaError_t gemm_prepare();   // per-device one-time kernel attributes
 // Rows of the A (gathered rows) box the projection uses for a batch of M tokens.
 int gemm_a_rows(int64_t M);
+// Whether the projection variant for M tokens has shared memory for the fused epilogue.
+bool gemm_can_fuse(int64_t M);
 // bf16 [rows, cols] row-major matrix, box = [box_rows, 64 columns], 128-byte swizzle.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 // rows: the gathered rows [M, K] (its tensor map is built here, to match the

@@ -52,7 +52,7 @@ class EngramLayer:
 
     def __init__(self, table, scale, wkv, q_weight, k_weight, *, dim=5120, hc_mult=4, n_cols=24, head_dim=256,
                  scale_block=128, scale_fmt=_lib.SCALE_F32, eps=1e-6, clamp=1e-6, max_tokens=4096,
-                 check_ids=False):
+                 check_ids=False, fuse_gate=False):
         dev = table.device
         if dev.type != "cuda":
             raise ValueError("the Engram layer runs on a CUDA device only")
@@ -71,7 +71,8 @@ class EngramLayer:
         self._keep = (table, scale, wkv, q_weight, k_weight)
         self.cfg = EngramConfig(dim=dim, hc_mult=hc_mult, n_cols=n_cols, head_dim=head_dim,
                                 scale_block=scale_block, scale_fmt=scale_fmt, num_rows=R, eps=eps, clamp=clamp,
-                                max_tokens=max_tokens, check_ids=1 if check_ids else 0)
+                                max_tokens=max_tokens, check_ids=1 if check_ids else 0,
+                                fuse_gate=1 if fuse_gate else 0)
         w = EngramWeights(table=_ptr(table), scale=_ptr(scale), wkv=_ptr(wkv), q_weight=_ptr(q_weight),
                           k_weight=_ptr(k_weight))
         self._ctx = ctypes.c_void_p()

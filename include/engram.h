@@ -89,6 +89,11 @@ typedef struct {
   float clamp;          /* lower clamp of |dot| before the square root (1e-6 in V4.1) */
   int32_t max_tokens;   /* largest B*T of any later call; sizes the scratch */
   int32_t check_ids;    /* non-zero: count ids outside [0, R) and report ENGRAM_ERANGE */
+  int32_t fuse_gate;    /* non-zero: when the projection runs without split-K, engram_forward
+                           forms the gate and the residual add in the projection's epilogue
+                           (kv never reaches HBM) instead of a separate kernel.  Same bits
+                           either way; on GB300 the separate kernel measured faster (the
+                           epilogue work slows the power-capped MMA), so 0 is the default. */
 } engram_config;
 
 typedef struct {
@@ -180,8 +185,8 @@ ENGRAM_API engram_status engram_stage_times(engram_ctx* ctx, float* ms);
  * of ENGRAM_NOALLOC_SCRATCH_BYTES bytes; the CUDA driver places it in device
  * memory when it loads this part of the library on a device, and every device
  * that loads it keeps those bytes until the process exits.
- *  - cfg and w are as for engram_create() (max_tokens and check_ids are
- *    ignored); the weights are read on every call.  Shapes with
+ *  - cfg and w are as for engram_create() (max_tokens, check_ids and
+ *    fuse_gate are ignored); the weights are read on every call.  Shapes with
  *    n_cols*head_dim > 6144 or dim*(hc_mult+1) > 25600 give ENGRAM_EUNSUPPORTED.
  *  - B*T > ENGRAM_NOALLOC_MAX_TOKENS gives ENGRAM_EINVAL and queues nothing.
  *  - The first call on each device looks up the device address of the scratch

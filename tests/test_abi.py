@@ -65,7 +65,7 @@ int main(void) {
   printf("engram_config %zu\n", sizeof(engram_config));
   F(engram_config, dim); F(engram_config, hc_mult); F(engram_config, n_cols); F(engram_config, head_dim);
   F(engram_config, scale_block); F(engram_config, scale_fmt); F(engram_config, num_rows); F(engram_config, eps);
-  F(engram_config, clamp); F(engram_config, max_tokens); F(engram_config, check_ids);
+  F(engram_config, clamp); F(engram_config, max_tokens); F(engram_config, check_ids); F(engram_config, fuse_gate);
   printf("engram_weights %zu\n", sizeof(engram_weights));
   F(engram_weights, table); F(engram_weights, scale); F(engram_weights, wkv); F(engram_weights, q_weight);
   F(engram_weights, k_weight);

@@ -188,3 +188,31 @@ def test_empty_batch_is_a_no_op(tiny):
     out = layer.forward(ids, x)
     assert out.shape == x.shape
     assert layer.sync_status()[0] == 0
+
+
+@pytest.mark.parametrize("B,T,mask_frac", [(1, 150, 0.1), (300, 1, 0.0), (7, 100, 0.3)])
+def test_fused_epilogue_matches_split_path(tiny, B, T, mask_frac):
+    """fuse_gate: the gate and residual add run in the projection's epilogue
+    (plans without split-K); the result must equal lookup_project + gate_apply
+    bit for bit, and match the oracle."""
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    dev = tiny["dev"]
+    fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=1024,
+                        fuse_gate=True)
+    w, inp = _inputs(tiny, B, T, mask_frac, seed=21)
+    ids, x, mask = _dev(inp)
+    out = fused.forward(ids, x, mask)
+    again = fused.forward(ids, x, mask)
+    kv = fused.lookup_project(ids)
+    gates = torch.empty((B, T, 4), dtype=torch.float32, device="cuda")
+    split = fused.gate_apply(kv, x, mask, gates=gates)
+    inplace = x.clone()
+    fused.forward(ids, inplace, mask, out=inplace)
+    assert fused.sync_status()[0] == 0
+    assert fused.plan(B * T)[0] == 1                      # the fused epilogue needs a plan without split-K
+    assert torch.equal(out.view(torch.int16), split.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), inplace.view(torch.int16))
+    M = B * T
+    P.check_layer(w, inp, np.arange(M), SD.device_bits(out), gates.cpu().numpy(), SD.device_bits(kv), "fused")
+    fused.close()
