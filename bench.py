@@ -333,12 +333,7 @@ def run_ours(args, w, rank, world, local_rank):
     d2h = inp.x.nbytes
 
     # ---- aggregate over ranks
-    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t[0]), float(t[1])
-    value = world * M * args.steps / (total_ms / 1e3)
-    e2e_value = world * M * args.steps / (e2e_ms / 1e3)
+    value, e2e_value, total_ms, e2e_ms = aggregate_over_ranks(total_ms, e2e_ms, M, args.steps, world, dev)
 
     pk = peaks()
     splits, ctas = layer.plan(M)
@@ -387,6 +382,21 @@ def run_ours(args, w, rank, world, local_rank):
         result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                                   "sample": desc, "seconds": el}
     return result
+
+
+def aggregate_over_ranks(total_ms, e2e_ms, tokens_per_rank, steps, world, device):
+    """Whole-job throughput of a weak-scaling run: every rank processed
+    tokens_per_rank tokens per step, and the job took as long as its slowest
+    rank (max over ranks of the timed milliseconds).  Returns (tokens/s,
+    e2e tokens/s, max timed ms, max e2e ms)."""
+    import torch
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t[0]), float(t[1])
+    tokens = world * tokens_per_rank * steps
+    return tokens / (total_ms / 1e3), tokens / (e2e_ms / 1e3), total_ms, e2e_ms
 
 
 def inp_pinned(torch, a):
