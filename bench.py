@@ -403,6 +403,43 @@ def inp_pinned(torch, a):
     return torch.from_numpy(a).pin_memory()
 
 
+def run_hash(args, w):
+    """Times engram_hash alone (two Engram layers, 3 orders x 8 heads, the 48
+    primes above 16,000,000, synthetic token ids and map) on the workload's
+    B x T; prints its own JSON line."""
+    import numpy as np
+    import torch
+    from engram_hashed_gram_gb300 import build as B
+    from engram_hashed_gram_gb300 import synth
+    from engram_hashed_gram_gb300.layer import EngramHasher
+    B.build()
+    rng = np.random.default_rng(w.seed)
+    vocab = 129_280
+    primes = np.array(synth.consecutive_primes_above(16_000_000, 48), dtype=np.int64).reshape(2, 3, 8)
+    offsets = np.stack([np.concatenate([[0], np.cumsum(primes[g].reshape(-1))[:-1]]) for g in range(2)])
+    mult = (rng.integers(1, 1 << 62, size=(2, 4)) * 2 + 1).astype(np.int64)
+    tmap = rng.integers(0, 99_092, size=vocab).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    hasher = EngramHasher(dev(tmap), dev(mult), dev(primes), dev(offsets), max_batch=w.B, max_len=w.T)
+    ids = dev(rng.integers(0, vocab, size=(w.B, w.T)))
+    out = torch.empty((2, w.B, w.T, 24), dtype=torch.int64, device="cuda")
+    for _ in range(args.warmup):
+        hasher(ids, 0, out=out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        hasher(ids, 0, out=out)
+        b.record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    per_tok = 8 + 4 + 2 * 24 * 8                     # ids read, cache write, ids of two layers written
+    return {"component": "engram_hash", "metric": "hashed tokens/s", "value": w.M / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "gbs": w.M * per_tok / (ms * 1e-3) / 1e9,
+            "bytes_per_token": per_tok, "config": {"workload": w.name, "B": w.B, "T": w.T, "n_layers": 2,
+                                                   "orders": [2, 3, 4], "heads": 8}}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,6 +449,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--component", choices=["layer", "hash"], default="layer",
+                    help="hash: time the n-gram hash (engram_hash) alone and print its own JSON line")
     ap.add_argument("--fuse-gate", action="store_true",
                     help="form the gate in the projection's epilogue (engram_config.fuse_gate)")
     ap.add_argument("--prime-base", type=int, default=None,
@@ -433,6 +472,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.component == "hash":
+        if rank == 0:
+            print(json.dumps(run_hash(args, w)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank == 0:

@@ -45,6 +45,19 @@ class EngramConfig(ctypes.Structure):
     ]
 
 
+class EngramHashConfig(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", c_int32),
+        ("max_ngram_size", c_int32),
+        ("n_heads", c_int32),
+        ("max_batch", c_int32),
+        ("max_len", c_int64),
+        ("vocab_size", c_int64),
+        ("pad_id", c_int32),
+        ("dead_id", c_int32),
+    ]
+
+
 class EngramWeights(ctypes.Structure):
     _fields_ = [
         ("table", c_void_p),
@@ -68,6 +81,8 @@ ENGRAM_FUNCS = {
     "engram_plan": (c_int32, [c_void_p, c_int64, POINTER(c_int32), POINTER(c_int32)]),
     "engram_forward_noalloc": (c_int32, [POINTER(EngramConfig), POINTER(EngramWeights), c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_int64, c_int64, c_void_p]),
+    "engram_hash": (c_int32, [POINTER(EngramHashConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                              c_void_p, c_int64, c_void_p, c_int64, c_int64, c_void_p]),
     "engram_enable_stage_timing": (c_int32, [c_void_p, c_int32]),
     "engram_stage_times": (c_int32, [c_void_p, POINTER(c_float)]),
     "engram_status_string": (c_char_p, [c_int32]),

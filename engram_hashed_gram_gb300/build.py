@@ -27,7 +27,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-
                      "-I", INCLUDE]
 
 LIBS = {
-    "libengram.so": ["gather.cu", "gemm.cu", "gate.cu", "engram_api.cu", "noalloc.cu"],
+    "libengram.so": ["gather.cu", "gemm.cu", "gate.cu", "engram_api.cu", "noalloc.cu", "hash.cu"],
     "libengram_synth.so": ["synth.cu"],
 }
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.cuh")] + \

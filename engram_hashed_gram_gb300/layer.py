@@ -12,7 +12,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import EngramConfig, EngramWeights, check
+from ._lib import EngramConfig, EngramHashConfig, EngramWeights, check
 
 _U16 = (torch.bfloat16, torch.int16, torch.uint16)
 
@@ -174,3 +174,47 @@ class EngramLayer:
             self.close()
         except Exception:
             pass
+
+
+class EngramHasher:
+    """The n-gram hash of every Engram layer of a model (include/engram.h,
+    engram_hash), with its session cache.
+
+    token_map: int32 [vocab]; multipliers: int64 [n_layers, max_ngram_size];
+    primes: int64 [n_layers, max_ngram_size-1, n_heads]; offsets: int64
+    [n_layers, (max_ngram_size-1)*n_heads]; all on one CUDA device.  The cache
+    ([max_batch, max_len] int32) is allocated here and holds each sequence's
+    compressed history between calls."""
+
+    def __init__(self, token_map, multipliers, primes, offsets, *, max_batch, max_len, pad_id=2, dead_id=-1):
+        dev = token_map.device
+        n_layers, n = multipliers.shape
+        heads = primes.shape[2]
+        _need(token_map, "token_map", (torch.int32,), None, dev)
+        _need(multipliers, "multipliers", (torch.int64,), (n_layers, n), dev)
+        _need(primes, "primes", (torch.int64,), (n_layers, n - 1, heads), dev)
+        _need(offsets, "offsets", (torch.int64,), (n_layers, (n - 1) * heads), dev)
+        self.device = dev
+        self.n_layers, self.cols = n_layers, (n - 1) * heads
+        self.cfg = EngramHashConfig(n_layers=n_layers, max_ngram_size=n, n_heads=heads, max_batch=max_batch,
+                                    max_len=max_len, vocab_size=token_map.numel(), pad_id=pad_id, dead_id=dead_id)
+        self.cache = torch.zeros((max_batch, max_len), dtype=torch.int32, device=dev)
+        self._keep = (token_map, multipliers, primes, offsets)
+        self._lib = _lib.engram()
+
+    def __call__(self, input_ids, start_pos=0, token_mask=None, out=None, stream=None):
+        """hash ids [n_layers, B, L, cols] for positions [start_pos, start_pos + L)."""
+        _need(input_ids, "input_ids", (torch.int64,), None, self.device)
+        B, L = input_ids.shape
+        if token_mask is not None:
+            if token_mask.dtype == torch.bool:
+                token_mask = token_mask.view(torch.uint8)
+            _need(token_mask, "token_mask", (torch.uint8,), (B, L), self.device)
+        if out is None:
+            out = torch.empty((self.n_layers, B, L, self.cols), dtype=torch.int64, device=self.device)
+        _need(out, "out", (torch.int64,), (self.n_layers, B, L, self.cols), self.device)
+        tm, mu, pr, of = self._keep
+        check(self._lib.engram_hash(ctypes.byref(self.cfg), _ptr(tm), _ptr(mu), _ptr(pr), _ptr(of), _ptr(self.cache),
+                                    _ptr(input_ids), _ptr(token_mask), start_pos, _ptr(out), B, L, _stream(stream)),
+              "engram_hash")
+        return out

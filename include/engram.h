@@ -167,6 +167,49 @@ ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, in
 ENGRAM_API engram_status engram_enable_stage_timing(engram_ctx* ctx, int32_t enable);
 ENGRAM_API engram_status engram_stage_times(engram_ctx* ctx, float* ms);
 
+/* ---- n-gram hash: the step before the layer ----------------------------------
+ * The hash `forward` excerpt of atlas.klimoza.dev "deepseek-v4.1 / engram-second"
+ * (and monishver11.github.io "DeepSeek's Other Modules", section "The lookup
+ * pipeline"): token ids -> the global table rows of every Engram layer.
+ *   1. c = token_map[id]; ids outside [0, vocab_size) and positions whose
+ *      token_mask is 0 become dead_id (they take part in no n-gram);
+ *   2. cache[b, start_pos + l] = c (the session's history of compressed ids);
+ *   3. look-back s = 0 .. max_ngram_size-1: the id s positions back; once a
+ *      look-back reaches before position 0 or a dead_id, it and every longer
+ *      one are pad_id;
+ *   4. with 64-bit wrapping products p_s = id_s * multipliers[g, s], the XOR of
+ *      p_0 .. p_i hashes the (i+1)-gram;
+ *   5. row = hash mod primes[g, i-1, h] (remainder with the divisor's sign) +
+ *      offsets[g, (i-1)*n_heads + h].
+ * Calls for one session must come in position order; a call may cover any
+ * chunk [start_pos, start_pos + L) of it (earlier positions are read from the
+ * cache). */
+typedef struct {
+  int32_t n_layers;        /* Engram layers that share the hash (2 in V4.1) */
+  int32_t max_ngram_size;  /* n-grams of 2 .. max_ngram_size tokens (4 in V4.1); 2..8 */
+  int32_t n_heads;         /* hash heads per n-gram order (8 in V4.1); 1..32 */
+  int32_t max_batch;       /* rows of the session cache */
+  int64_t max_len;         /* positions per cache row */
+  int64_t vocab_size;      /* entries of token_map */
+  int32_t pad_id;          /* id of a blocked look-back (engram_pad_id, 2 in V4.1) */
+  int32_t dead_id;         /* id of a position in no n-gram (e.g. -1) */
+} engram_hash_config;
+
+/* All pointers are device pointers, caller-owned.  token_map: [vocab_size]
+ * int32; multipliers: [n_layers, max_ngram_size] int64; primes: [n_layers,
+ * max_ngram_size-1, n_heads] int64 (positive); offsets: [n_layers,
+ * (max_ngram_size-1)*n_heads] int64; cache: [max_batch, max_len] int32, the
+ * session state (read below start_pos, written at [start_pos, start_pos+L));
+ * input_ids: [B, L] int64; token_mask: [B, L] uint8 or NULL; hash_ids:
+ * [n_layers, B, L, (max_ngram_size-1)*n_heads] int64 -- hash_ids[g] is the id
+ * array of Engram layer g for engram_forward.  B <= max_batch and start_pos + L
+ * <= max_len, else ENGRAM_EINVAL.  Asynchronous on `stream`. */
+ENGRAM_API engram_status engram_hash(const engram_hash_config* cfg, const int32_t* token_map,
+                                     const int64_t* multipliers, const int64_t* primes, const int64_t* offsets,
+                                     int32_t* cache, const int64_t* input_ids, const uint8_t* token_mask,
+                                     int64_t start_pos, int64_t* hash_ids, int64_t B, int64_t L,
+                                     engram_stream_t stream);
+
 /* ---- allocation-free variant ------------------------------------------------
  * The pages have no counterpart to this entry point; it exists for callers of
  * this library that cannot allocate device memory.  A serving engine that

@@ -69,6 +69,10 @@ int main(void) {
   printf("engram_weights %zu\n", sizeof(engram_weights));
   F(engram_weights, table); F(engram_weights, scale); F(engram_weights, wkv); F(engram_weights, q_weight);
   F(engram_weights, k_weight);
+  printf("engram_hash_config %zu\n", sizeof(engram_hash_config));
+  F(engram_hash_config, n_layers); F(engram_hash_config, max_ngram_size); F(engram_hash_config, n_heads);
+  F(engram_hash_config, max_batch); F(engram_hash_config, max_len); F(engram_hash_config, vocab_size);
+  F(engram_hash_config, pad_id); F(engram_hash_config, dead_id);
   return 0;
 }
 ''')
@@ -78,8 +82,10 @@ int main(void) {
     c = dict(l.rsplit(" ", 1) for l in lines if l)
     assert int(c["engram_config"]) == ctypes.sizeof(libs.EngramConfig)
     assert int(c["engram_weights"]) == ctypes.sizeof(libs.EngramWeights)
-    for T in (libs.EngramConfig, libs.EngramWeights):
-        cname = "engram_config" if T is libs.EngramConfig else "engram_weights"
+    assert int(c["engram_hash_config"]) == ctypes.sizeof(libs.EngramHashConfig)
+    names = {libs.EngramConfig: "engram_config", libs.EngramWeights: "engram_weights",
+             libs.EngramHashConfig: "engram_hash_config"}
+    for T, cname in names.items():
         for f, _ in T._fields_:
             assert int(c[f"{cname}.{f}"]) == getattr(T, f).offset, f
 
@@ -105,6 +111,7 @@ def test_host_only_entry_points(libs):
     assert lib.engram_plan(None, 1, None, None) == -1
     assert lib.engram_enable_stage_timing(None, 1) == -1
     assert lib.engram_stage_times(None, None) == -1
+    assert lib.engram_hash(None, None, None, None, None, None, None, None, 0, None, 1, 1, None) == -1
     lib.engram_destroy(None)
     syn = libs.synth()
     assert syn.engram_synth_fill_table(None, None, 0, 1, 256, 128, 0, 0, None, None, None) == -1
