@@ -203,7 +203,9 @@ typedef struct {
  * input_ids: [B, L] int64; token_mask: [B, L] uint8 or NULL; hash_ids:
  * [n_layers, B, L, (max_ngram_size-1)*n_heads] int64 -- hash_ids[g] is the id
  * array of Engram layer g for engram_forward.  B <= max_batch and start_pos + L
- * <= max_len, else ENGRAM_EINVAL.  Asynchronous on `stream`. */
+ * <= max_len, else ENGRAM_EINVAL; more than 6144 primes (n_layers *
+ * (max_ngram_size-1) * n_heads) give ENGRAM_EUNSUPPORTED.  Asynchronous on
+ * `stream`. */
 ENGRAM_API engram_status engram_hash(const engram_hash_config* cfg, const int32_t* token_map,
                                      const int64_t* multipliers, const int64_t* primes, const int64_t* offsets,
                                      int32_t* cache, const int64_t* input_ids, const uint8_t* token_mask,

@@ -112,6 +112,12 @@ def test_host_only_entry_points(libs):
     assert lib.engram_enable_stage_timing(None, 1) == -1
     assert lib.engram_stage_times(None, None) == -1
     assert lib.engram_hash(None, None, None, None, None, None, None, None, 0, None, 1, 1, None) == -1
+    # more primes than the kernel's shared-memory table holds, refused before any CUDA call
+    hc = libs.EngramHashConfig(n_layers=97, max_ngram_size=3, n_heads=32, max_batch=1, max_len=1, vocab_size=1,
+                               pad_id=2, dead_id=-1)
+    assert lib.engram_hash(ctypes.byref(hc), None, None, None, None, None, None, None, 0, None, 0, 0, None) == -6
+    hc.n_layers = 96                                        # 96 * 2 * 32 = 6144 primes: accepted, empty batch
+    assert lib.engram_hash(ctypes.byref(hc), None, None, None, None, None, None, None, 0, None, 0, 0, None) == 0
     lib.engram_destroy(None)
     syn = libs.synth()
     assert syn.engram_synth_fill_table(None, None, 0, 1, 256, 128, 0, 0, None, None, None) == -1

@@ -60,6 +60,25 @@ def test_hash_matches_oracle_over_chunked_calls(built, n_layers, n, heads):
     assert np.array_equal(hasher.cache[:B, :Ltot].cpu().numpy(), cache[:B, :Ltot])
 
 
+def test_extreme_divisors(built):
+    """The remainder for divisors from 1 to 2^63-1 (powers of two, 2^32 +- 1,
+    the largest int64) on hashes that cover the whole int64 range, including
+    its most negative value (multiplier 2^63 with an odd id)."""
+    from engram_hashed_gram_gb300.layer import EngramHasher
+    rng = np.random.default_rng(63)
+    divisors = np.array([1, 2, 3, 7, 1 << 20, (1 << 31) - 1, (1 << 32) - 1, 1 << 32, (1 << 32) + 1,
+                         (1 << 40) + 7, (1 << 62) - 57, 1 << 62, (1 << 62) + 135, (1 << 63) - 25,
+                         (1 << 63) - 1, 16_000_057], dtype=np.int64).reshape(2, 1, 8)
+    token_map, mult, primes, offsets = _params(rng, 2, 2, 8, 500, primes=divisors)
+    mult[0, 1] = np.int64(-(1 << 63))                       # products 0 or INT64_MIN
+    offsets[:] = 0                                          # the divisors' sums overflow int64
+    ids = rng.integers(0, 500, size=(4, 64))
+    hasher = EngramHasher(*_dev(token_map, mult, primes, offsets), max_batch=4, max_len=64)
+    got = hasher(torch.from_numpy(ids).cuda()).cpu().numpy()
+    want = H.ngram_hash(ids, 0, np.zeros((4, 64), np.int64), token_map, mult, primes, offsets, 2, -1)
+    assert np.array_equal(got, np.transpose(want, (2, 0, 1, 3)))
+
+
 def test_v41_layout(built):
     """Two layers, 3 orders x 8 heads, the 48 primes above 16,000,000 (first 24
     for the first module, next 24 for the second); every id lies in its
