@@ -105,6 +105,18 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* map
       : "memory");
 }
 
+// Contiguous bulk copy global -> shared memory of `bytes` (both addresses 16-byte
+// aligned, a multiple of 16 bytes), counted on `bar`'s transaction count, with
+// an L2 eviction-priority policy.
+__device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

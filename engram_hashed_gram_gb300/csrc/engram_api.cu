@@ -31,6 +31,7 @@ struct engram_ctx {
   float* gsum;                // [max_tokens, hc, dim/256, 4] fused-epilogue block sums
   float* gates;               // [max_tokens, 4] fused-epilogue gates
   uint32_t* counters;         // [ceil(max_tokens/128), 8] fused-epilogue counters and flags
+  uint8_t* wpack;             // wkv in 32 KB swizzled tiles (launch_pack_wkv), N*K*2 bytes
   CUtensorMap tmW;
   cudaEvent_t ev[4];          // stage timing (null unless enabled)
   bool timing;
@@ -163,6 +164,7 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
   a.kv = kv_out;
   a.part = c->part;
   a.err = c->err;
+  a.wpack = c->wpack;
   if (fuse) {
     a.out_mode = kOutFused;
     a.x = fused->x;
@@ -213,6 +215,7 @@ void free_ctx(engram_ctx* c) {
   cudaFree(c->gsum);
   cudaFree(c->counters);
   cudaFree(c->gates);
+  cudaFree(c->wpack);
   delete c;
 }
 
@@ -286,7 +289,8 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
                 cudaSuccess &&
             cudaMalloc(&ctx->counters, static_cast<size_t>((mt + kBM - 1) / kBM) * 8 * sizeof(uint32_t)) ==
                 cudaSuccess &&
-            cudaMalloc(&ctx->gates, static_cast<size_t>(mt) * 4 * sizeof(float)) == cudaSuccess;
+            cudaMalloc(&ctx->gates, static_cast<size_t>(mt) * 4 * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&ctx->wpack, static_cast<size_t>(N) * K * 2) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_ctx(ctx);
@@ -295,6 +299,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
   if (cudaMemset(ctx->err, 0, 2 * sizeof(unsigned long long)) != cudaSuccess ||
       launch_weight_product(w->q_weight, w->k_weight, ctx->wprod, static_cast<int64_t>(hcd), nullptr) !=
           cudaSuccess ||
+      launch_pack_wkv(w->wkv, N, K, ctx->wpack, nullptr) != cudaSuccess ||
       gemm_prepare() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     free_ctx(ctx);
     return ENGRAM_ECUDA;

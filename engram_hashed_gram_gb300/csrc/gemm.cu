@@ -23,6 +23,7 @@
 // whatever the neighbouring shared memory holds, their accumulator rows are
 // never stored, and a row of D depends on its own row of A only.  Rows of the
 // last M tile past M read as zeros (TMA bounds fill) and are not stored.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -77,10 +78,11 @@ __device__ __forceinline__ void raster(const GemmArgs& a, int64_t t, int n_count
 // before every value tile: a value tile waits only for units with smaller
 // indices, and by the time any CTA reaches the value tiles nearly all key
 // tiles are done.
+template <bool FUSED>
 __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& mt, int& nt, int& sp) {
   sp = static_cast<int>(u % a.splits);
   const int64_t t = u / a.splits;
-  if (a.out_mode == kOutFused) {
+  if constexpr (FUSED) {
     const int64_t key_units = static_cast<int64_t>(a.m_tiles) * a.key_n_tiles;
     if (t < key_units) {
       raster(a, t, a.key_n_tiles, mt, nt);
@@ -91,6 +93,18 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& m
     return;
   }
   raster(a, t, a.n_tiles, mt, nt);
+}
+
+// The weight tile (N tile nt, K block kb) into a B stage: one contiguous 32 KB
+// copy from the packed weight, or a 2-D tensor copy of the row-major weight.
+__device__ __forceinline__ void load_b(const GemmArgs& a, const CUtensorMap& tmB, uint8_t* dst, uint64_t* bar, int nt,
+                                       int kb, uint64_t policy) {
+  if (a.wpack != nullptr) {
+    const int64_t tile = static_cast<int64_t>(nt) * (a.K / kBK) + kb;
+    bulk_load_hint(dst, a.wpack + tile * kBBytes, kBBytes, bar, policy);
+  } else {
+    tma_load_2d_hint(dst, &tmB, bar, kb * kBK, nt * kBN, policy);
+  }
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned long long* err) {
@@ -349,7 +363,9 @@ __device__ __forceinline__ bool fused_value_epilogue(const GemmArgs& a, uint32_t
   return true;
 }
 
-template <int A_ROWS, int STAGES>
+// FUSED selects the gate epilogue at compile time, so that the plain kernel
+// carries none of its registers.
+template <int A_ROWS, int STAGES, bool FUSED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
@@ -412,11 +428,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int pre = 0;
       if (static_cast<int64_t>(blockIdx.x) < a.units) {
         int mt, nt, sp;
-        unit_coords(a, blockIdx.x, mt, nt, sp);
+        unit_coords<FUSED>(a, blockIdx.x, mt, nt, sp);
         pre = min(kStages, a.kb_per_split);
         for (int i = 0; i < pre; ++i) {   // fresh ring: every stage is free
           mbar_arrive_expect_tx(&full[i], kStageBytes);
-          tma_load_2d_hint(smB + i * kBBytes, &tmB, &full[i], (sp * a.kb_per_split + i) * kBK, nt * kBN, pol_w);
+          load_b(a, tmB, smB + i * kBBytes, &full[i], nt, sp * a.kb_per_split + i, pol_w);
         }
       }
       grid_dependency_wait();     // the gathered rows are written by the gather kernel
@@ -425,7 +441,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // every CTA has begun its last unit
         if (u + gridDim.x >= a.units) grid_launch_dependents();
         int mt, nt, sp;
-        unit_coords(a, u, mt, nt, sp);
+        unit_coords<FUSED>(a, u, mt, nt, sp);
         const int kb0 = sp * a.kb_per_split;
         for (int kb = 0; kb < a.kb_per_split; ++kb) {
           if (u == blockIdx.x && kb < pre) {
@@ -438,7 +454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             mbar_arrive_expect_tx(&full[stage], kStageBytes);
             tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], (kb0 + kb) * kBK, mt * kBM);
-            tma_load_2d_hint(smB + stage * kBBytes, &tmB, &full[stage], (kb0 + kb) * kBK, nt * kBN, pol_w);
+            load_b(a, tmB, smB + stage * kBBytes, &full[stage], nt, kb0 + kb, pol_w);
           }
           ++issued[stage];
           if (++stage == kStages) {
@@ -514,7 +530,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       if (u + gridDim.x >= a.units) grid_launch_dependents();
       int mt, nt, sp;
-      unit_coords(a, u, mt, nt, sp);
+      unit_coords<FUSED>(a, u, mt, nt, sp);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         break;
@@ -522,7 +538,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      if (a.out_mode != kOutFused) {
+      if constexpr (!FUSED) {
         plain_epilogue(a, t_row, m, nt, sp);
       } else if (nt < a.key_n_tiles) {
         fused_key_epilogue(a, t_row, m, nt * kBN, lane, reinterpret_cast<float*>(epi));
@@ -550,8 +566,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int A_ROWS, int STAGES>
 cudaError_t set_smem_attr() {
   using C = Cfg<A_ROWS, STAGES>;
-  return cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(C::kCanFuse ? C::kSmemFused : C::kSmemBytes));
+  cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
+  if (e == cudaSuccess && C::kCanFuse)
+    e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmemFused));
+  return e;
 }
 
 template <int A_ROWS, int STAGES>
@@ -559,9 +579,29 @@ cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            cudaStream_t stream) {
   using C = Cfg<A_ROWS, STAGES>;
   const bool fused = a.out_mode == kOutFused;
-  if (fused && !C::kCanFuse) return cudaErrorInvalidConfiguration;
-  return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES>, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads),
-                    fused ? C::kSmemFused : C::kSmemBytes, stream, 1, tmA, tmB, a);
+  if (!fused)
+    return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, false>, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads),
+                      C::kSmemBytes, stream, 1, tmA, tmB, a);
+  if (!C::kCanFuse) return cudaErrorInvalidConfiguration;
+  return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, true>, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads),
+                    C::kSmemFused, stream, 1, tmA, tmB, a);
+}
+
+// One thread per 16-byte chunk of the packed weight: chunk p of row r of a tile
+// holds the row's logical chunk p ^ (r % 8), the 128-byte swizzle.
+__global__ void __launch_bounds__(256) pack_wkv_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t chunks,
+                                                       uint4* __restrict__ out) {
+  const int64_t kb_total = K / kBK;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < chunks;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = i >> 11;                     // 2048 chunks of 16 bytes per 32 KB tile
+    const int r = static_cast<int>((i >> 3) & 255);
+    const int c = static_cast<int>(i & 7) ^ (r & 7);
+    const int64_t nt = tile / kb_total;
+    const int64_t kb = tile - nt * kb_total;
+    const int64_t n = nt * kBN + r;
+    out[i] = __ldg(reinterpret_cast<const uint4*>(w + n * K + kb * kBK + c * 8));
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -604,6 +644,15 @@ cudaError_t gemm_prepare() {
   if (e == cudaSuccess) e = set_smem_attr<64, 5>();
   if (e == cudaSuccess) e = set_smem_attr<32, 6>();
   return e;
+}
+
+cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream) {
+  if (N % kBN != 0 || K % kBK != 0) return cudaErrorInvalidValue;
+  const int64_t chunks = N * K / 8;
+  if (chunks == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((chunks + 255) / 256, 65536);
+  pack_wkv_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(wkv, K, chunks, reinterpret_cast<uint4*>(packed));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const uint16_t* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,

@@ -76,6 +76,7 @@ struct GemmArgs {
   int32_t group_m;       // m-tiles per rasterisation group
   int64_t units;         // m_tiles * n_tiles * splits
   int32_t out_mode;      // GemmOut
+  const uint8_t* wpack;  // the weight in tile-packed order (pack_wkv), or nullptr: read through tmB
   uint16_t* kv;          // kOutBf16: [M, N]
   float* part;           // kOutPartial: [splits, M, N]
   unsigned long long* err;
@@ -105,6 +106,12 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 // kernel variant); tmB: the weight's map, box [256 rows, 64 columns].
 cudaError_t launch_gemm(const uint16_t* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
                         cudaStream_t stream);
+// The weight [N, K] (N a multiple of 256, K of 64) rewritten as 32 KB tiles,
+// tile (n_tile, k_block) at byte offset (n_tile * K/64 + k_block) * 32768, each
+// holding rows n_tile*256 .. +255, columns k_block*64 .. +63 exactly as a
+// 128-byte-swizzled tensor copy of that box lands in shared memory.  `packed`
+// holds N*K*2 bytes, 16-byte aligned.
+cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream);
 
 // ---- gate and residual (steps a5-a8) ---------------------------------------
 struct GateArgs {

@@ -110,8 +110,13 @@ typedef struct engram_ctx engram_ctx;
 
 /* Validates the configuration, allocates the context's scratch on the current
  * device (sized by max_tokens), forms the fp32 product q_weight*k_weight
- * (used only as a product, per the `Engram` excerpt) and builds the tensor-map
- * descriptor of wkv.  The weights are referenced, not copied.  Synchronous.
+ * (used only as a product, per the `Engram` excerpt) and copies wkv into a
+ * buffer of its own (N*K*2 bytes) in 32 KB tiles of 256 rows x 64 columns,
+ * each stored as the projection's shared-memory stage holds it, so that every
+ * weight read of a forward call is one contiguous 32 KB stream.  The table and
+ * scales are referenced, not copied, and must outlive the context; wkv,
+ * q_weight and k_weight are read only here (a changed weight needs a new
+ * context).  Synchronous.
  * Returns ENGRAM_EINVAL / ENGRAM_EUNSUPPORTED for bad or unsupported shapes,
  * ENGRAM_ENOMEM if the scratch cannot be allocated, ENGRAM_ECUDA otherwise. */
 ENGRAM_API engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w);
