@@ -40,6 +40,8 @@ import numpy as np
 
 SCALE_F32 = 0
 SCALE_E8M0 = 1
+WKV_BF16 = 0
+WKV_MXFP8 = 1
 
 
 # --------------------------------------------------------------------------
@@ -162,6 +164,32 @@ def project(e_bits, wkv_bits) -> np.ndarray:
     return round_to_bf16(e @ w.T)
 
 
+def mxfp8_weight(codes, scales, block: int = 32) -> np.ndarray:
+    """The projection weight in the V4.1 FP8 format -> float64 [N, K], exact:
+    W[j, k] = e4m3(codes[j, k]) * 2^(scales[j, k // block] - 127).
+
+    monishver11.github.io "DeepSeek's Other Modules", section "V4.1's two
+    tables, reconciled", says the tables and the projections are FP8, and
+    zhuai.tech "Engram in DeepSeek V4.1 Flash" (section "Step 2: Read selected
+    rows ...") describes the tables' MXFP8 format: E4M3 codes with one E8M0
+    scale per 32 values.  The reading taken for the weight is the same format
+    along its input dimension K (one scale per 32 consecutive inputs of an
+    output row).  codes: uint8 [N, K]; scales: uint8 [N, K/block]."""
+    c = np.asarray(codes, dtype=np.uint8)
+    N, K = c.shape
+    s = decode_e8m0(np.asarray(scales, dtype=np.uint8).reshape(N, K // block))
+    return (decode_e4m3(c).reshape(N, K // block, block) * s[:, :, None]).reshape(N, K)
+
+
+def project_mxfp8(e_bits, w_codes, w_scales, block: int = 32) -> np.ndarray:
+    """kv = wkv(e) with the FP8 weight: kv[m, j] = bf16( sum_k e[m, k] * W[j, k] ),
+    W = mxfp8_weight(w_codes, w_scales).  Products of a bf16 value and a
+    block-scaled e4m3 value are exact in float64; the sum is taken in float64
+    (a library matrix product) and rounded once."""
+    e = bf16_value(e_bits)
+    return round_to_bf16(e @ mxfp8_weight(w_codes, w_scales, block).T)
+
+
 # --------------------------------------------------------------------------
 # a5-a7: split, gate reductions, gate
 # --------------------------------------------------------------------------
@@ -217,19 +245,21 @@ def residual(kv_bits, x_bits, g, mask=None) -> np.ndarray:
 # --------------------------------------------------------------------------
 def forward(hash_ids, x_bits, table, scale, wkv_bits, q_bits, k_bits, mask=None,
             scale_block: int = 128, scale_fmt: int = SCALE_F32, eps: float = 1e-6,
-            clamp: float = 1e-6):
+            clamp: float = 1e-6, wkv_scale=None):
     """Engram layer: returns (out bf16 bits [M, hc, dim], gates float64 [M, hc],
     kv bf16 bits [M, dim*(hc+1)]).
 
     hash_ids: int64 [M, n_cols]; x_bits: uint16 [M, hc, dim]; table: uint8
     [R, head_dim]; scale: [R, head_dim/scale_block]; wkv_bits: uint16
     [dim*(hc+1), n_cols*head_dim]; q_bits, k_bits: uint16 [hc, dim]; mask:
-    [M] truthy = apply, or None."""
+    [M] truthy = apply, or None.  With wkv_scale given, wkv_bits holds the
+    weight's e4m3 codes (uint8, same shape) and wkv_scale its E8M0 scales
+    [dim*(hc+1), n_cols*head_dim/32] (project_mxfp8)."""
     x_bits = np.asarray(x_bits, dtype=np.uint16)
     M = x_bits.shape[0]
     ids = np.asarray(hash_ids, dtype=np.int64).reshape(M, -1)
     e = lookup(ids, table, scale, scale_block, scale_fmt)
-    kv = project(e, wkv_bits)
+    kv = project(e, wkv_bits) if wkv_scale is None else project_mxfp8(e, wkv_bits, wkv_scale)
     g = gates(kv, x_bits, q_bits, k_bits, mask, eps, clamp)
     out = residual(kv, x_bits, g, mask)
     return out, g, kv

@@ -11,6 +11,7 @@ _orig_gates = O.gates
 _orig_residual = O.residual
 _orig_dequant = O.dequant_rows
 _orig_lookup = O.lookup
+_orig_mxfp8_weight = O.mxfp8_weight
 
 
 def _gates_variant(no_dim_scale=False, joint=False, no_clamp=False, q_only=False,
@@ -81,6 +82,28 @@ def _lookup_transposed(hash_ids, table, scale, scale_block, scale_fmt=O.SCALE_F3
     return e.reshape(M, C, hd).transpose(0, 2, 1).reshape(M, C * hd)
 
 
+def _mxfp8_block_64(codes, scales, block=32):
+    c = np.asarray(codes, dtype=np.uint8)
+    N, K = c.shape
+    s = O.decode_e8m0(np.asarray(scales, dtype=np.uint8).reshape(N, -1))
+    idx = np.minimum(np.arange(K) // 64, s.shape[1] - 1)          # one scale per 64 inputs
+    return O.decode_e4m3(c) * s[:, idx]
+
+
+def _mxfp8_scale_interleaved(codes, scales, block=32):
+    c = np.asarray(codes, dtype=np.uint8)
+    N, K = c.shape
+    s = O.decode_e8m0(np.asarray(scales, dtype=np.uint8).reshape(N, -1))
+    return O.decode_e4m3(c) * s[:, np.arange(K) % s.shape[1]]
+
+
+def _mxfp8_no_bias(codes, scales, block=32):
+    c = np.asarray(codes, dtype=np.uint8)
+    N, K = c.shape
+    s = np.ldexp(1.0, np.asarray(scales, dtype=np.int64).reshape(N, -1) - 126)   # bias off by one
+    return O.decode_e4m3(c) * s[:, np.arange(K) // block]
+
+
 def _round_truncate(x):
     x = np.asarray(x, dtype=np.float64)
     return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
@@ -100,6 +123,9 @@ MUTATIONS = {
     "dequant: product not rounded to fp32": ("dequant_rows", _dequant_double_product),
     "lookup: transposed flatten": ("lookup", _lookup_transposed),
     "bf16: truncation": ("round_to_bf16", _round_truncate),
+    "mxfp8 weight: one scale per 64": ("mxfp8_weight", _mxfp8_block_64),
+    "mxfp8 weight: scales interleaved": ("mxfp8_weight", _mxfp8_scale_interleaved),
+    "mxfp8 weight: E8M0 bias off by one": ("mxfp8_weight", _mxfp8_no_bias),
 }
 
 PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_") and n != "test_forward_tiny_vs_torch_restatement"]

@@ -212,6 +212,69 @@ def test_project_brute_force_exact_sums():
             assert Fraction(float(got)) / ulp == int(Fraction(float(got)) / ulp)
 
 
+def _e4m3_library(codes):
+    """e4m3 codes -> float64 through torch's float8_e4m3fn widening."""
+    c = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_mxfp8_weight_identity_copies_inputs():
+    """One 1.0 per output row (code 0x38, scale 2^0) makes the FP8 projection
+    a bit-exact copy of the chosen input channels; a scale one step up doubles
+    every value exactly."""
+    rng = np.random.default_rng(11)
+    M, K, N = 4, 128, 96
+    e = bf16_bits(rng.standard_normal((M, K)))
+    perm = (5 * np.arange(N) + 1) % K
+    codes = np.zeros((N, K), dtype=np.uint8)
+    codes[np.arange(N), perm] = 0x38
+    scales = np.full((N, K // 32), 127, dtype=np.uint8)
+    assert np.array_equal(O.project_mxfp8(e, codes, scales), e[:, perm])
+    up = O.bf16_value(O.project_mxfp8(e, codes, scales + 1))
+    assert np.array_equal(up, 2.0 * O.bf16_value(e[:, perm]))
+
+
+def test_mxfp8_block_scales_closed_form():
+    """All-ones input and weight codes 1.0 with scale 2^(b mod 5 - 2) on block
+    b: kv = 32 * sum_b 2^(b mod 5 - 2), one scale per 32 consecutive inputs."""
+    K, N = 320, 7
+    e = bf16_bits(np.ones((1, K)))
+    codes = np.full((N, K), 0x38, dtype=np.uint8)
+    nb = K // 32
+    scales = np.tile((127 + (np.arange(nb) % 5) - 2).astype(np.uint8), (N, 1))
+    scales[3] = 127                                             # one row unscaled
+    kv = O.bf16_value(O.project_mxfp8(e, codes, scales))
+    want = 32 * sum(2.0 ** ((b % 5) - 2) for b in range(nb))
+    assert np.all(kv[0, [0, 1, 2, 4, 5, 6]] == want)
+    assert kv[0, 3] == 32 * nb
+
+
+def test_mxfp8_projection_brute_force():
+    """Random codes (both signs, subnormals included) and scales against exact
+    rational sums of torch-widened codes times 2^(s-127), rounded once."""
+    rng = np.random.default_rng(12)
+    M, K, N = 3, 96, 11
+    e = bf16_bits(rng.standard_normal((M, K)))
+    codes = rng.integers(0, 256, size=(N, K)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3A                       # no NaN codes
+    scales = rng.integers(120, 134, size=(N, K // 32)).astype(np.uint8)
+    kv = O.bf16_value(O.project_mxfp8(e, codes, scales))
+    ev = O.bf16_value(e)
+    wv = _e4m3_library(codes)
+    for m in range(M):
+        for j in range(N):
+            exact = sum((Fraction(float(ev[m, k])) * Fraction(float(wv[j, k]))
+                         * Fraction(2) ** (int(scales[j, k // 32]) - 127) for k in range(K)), Fraction(0))
+            got = Fraction(float(kv[m, j]))
+            x = float(exact)
+            if x == 0.0:
+                assert got == 0
+                continue
+            _, ex = math.frexp(x)
+            ulp = Fraction(2) ** (ex - 8)
+            assert abs(got - exact) <= ulp / 2
+
+
 # ---------------------------------------------------------------------------
 # a6-a7: gate
 # ---------------------------------------------------------------------------
