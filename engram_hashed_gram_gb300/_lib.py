@@ -26,6 +26,8 @@ NOALLOC_SCRATCH_BYTES = 20529408  # ENGRAM_NOALLOC_SCRATCH_BYTES
 
 SCALE_F32 = 0
 SCALE_E8M0 = 1
+WKV_BF16 = 0
+WKV_MXFP8 = 1
 
 
 class EngramConfig(ctypes.Structure):
@@ -42,6 +44,7 @@ class EngramConfig(ctypes.Structure):
         ("max_tokens", c_int32),
         ("check_ids", c_int32),
         ("fuse_gate", c_int32),
+        ("wkv_fmt", c_int32),
     ]
 
 
@@ -65,6 +68,7 @@ class EngramWeights(ctypes.Structure):
         ("wkv", c_void_p),
         ("q_weight", c_void_p),
         ("k_weight", c_void_p),
+        ("wkv_scale", c_void_p),
     ]
 
 
@@ -92,6 +96,8 @@ ENGRAM_FUNCS = {
 SYNTH_FUNCS = {
     "engram_synth_fill_table": (c_int32, [c_void_p, c_void_p, c_int64, c_int64, c_int32, c_int32, c_uint64, c_uint64,
                                           c_void_p, c_void_p, c_void_p]),
+    "engram_synth_fill_scales_e8m0": (c_int32, [c_void_p, c_int64, c_int64, c_int32, c_int32, c_uint64, c_void_p,
+                                                c_void_p]),
 }
 
 _LIBS: dict[str, ctypes.CDLL] = {}

@@ -216,6 +216,49 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- block-scaled FP8
+// D[tmem] (+)= (A * sfA) * (B * sfB)^T with e4m3 A and B (K = 32 per
+// instruction) and one E8M0 scale per 32 K per row of A and of B, read from
+// tensor memory at sfa_tmem / sfb_tmem; fp32 accumulator, one CTA.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies a 32-row x 16-byte shared-memory tile into tensor memory lanes 0-31,
+// columns [col, col+4), and the same data into lanes 32-63, 64-95 and 96-127.
+// Asynchronous; a tcgen05.mma issued later by the same thread sees it.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// Descriptor of an unswizzled shared-memory tile of 16-byte rows (8-row core
+// matrices of 128 contiguous bytes, stacked 128 bytes apart): start address
+// >> 4, both byte offsets 128 >> 4, version 1, layout type 0 (no swizzle).
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: B scale-factor
+// id (which byte of the 32-bit scale column) in bits 4-5, A and B formats in
+// bits 7-9 and 10-12 (0 = e4m3), both K-major, N >> 3 in bits 17-22, scale
+// type in bit 23 (1 = UE8M0), M >> 4 in bits 24-28, A scale-factor id in bits
+// 29-30.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t m, uint32_t n, uint32_t sf_id) {
+  return (sf_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) | (sf_id << 29);
+}
+
 // ---------------------------------------------------------------- PDL
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -31,7 +31,11 @@ struct engram_ctx {
   float* gsum;                // [max_tokens, hc, dim/256, 4] fused-epilogue block sums
   float* gates;               // [max_tokens, 4] fused-epilogue gates
   uint32_t* counters;         // [ceil(max_tokens/128), 8] fused-epilogue counters and flags
-  uint8_t* wpack;             // wkv in 32 KB swizzled tiles (launch_pack_wkv), N*K*2 bytes
+  uint8_t* wpack;             // wkv in 32 KB swizzled tiles (launch_pack_wkv): N*K*2 bytes, N*K for MXFP8
+  bool fp8;                   // MXFP8 weight: block-scaled FP8 projection
+  uint8_t* wsf;               // fp8: the weight's scales, packed (launch_pack_sfb), N*K/32 bytes
+  uint8_t* codes;             // fp8: [max_tokens, K] gathered e4m3 codes
+  uint8_t* sfa;               // fp8: [ceil(max_tokens/128), K/128, 512] gathered scales
   CUtensorMap tmW;
   cudaEvent_t ev[4];          // stage timing (null unless enabled)
   bool timing;
@@ -56,7 +60,7 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
   Plan p{};
   p.m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
   p.n_tiles = c->N / kBN;
-  const int32_t kbt = c->K / kBK;
+  const int32_t kbt = c->K / (c->fp8 ? 128 : kBK);
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   auto waves = [&](int64_t units) { return (units + c->num_sms - 1) / c->num_sms; };
   int32_t best = 1;
@@ -132,7 +136,7 @@ struct FusedIO {
   uint16_t* out;
 };
 
-bool fuses(const Plan& p, int64_t M) { return p.splits == 1 && gemm_can_fuse(M); }
+bool fuses(const engram_ctx* c, const Plan& p, int64_t M) { return !c->fp8 && p.splits == 1 && gemm_can_fuse(M); }
 
 // gathered rows -> projection.  With `fused` and a fusable plan it writes the
 // layer's output; otherwise bf16 kv to kv_out when splits == 1 and the fp32
@@ -141,21 +145,26 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
                              Plan* plan_out, cudaStream_t stream) {
   if (cudaSetDevice(c->device) != cudaSuccess) return ENGRAM_ECUDA;
   const Plan p = make_plan(c, M);
-  const bool fuse = fused != nullptr && c->cfg.fuse_gate && fuses(p, M);
+  const bool fuse = fused != nullptr && c->cfg.fuse_gate && fuses(c, p, M);
   GatherArgs g = gather_args(c, ids, c->rows, M);
   if (fuse) {
     g.zero = c->counters;
     g.n_zero = p.m_tiles * 8;
   }
   mark(c, 0, stream);
-  if (launch_gather(g, c->num_sms, stream) != cudaSuccess) return ENGRAM_ECUDA;
+  if (c->fp8) {
+    if (launch_gather_codes(g, c->cfg.n_cols, c->codes, c->sfa, c->num_sms, stream) != cudaSuccess)
+      return ENGRAM_ECUDA;
+  } else if (launch_gather(g, c->num_sms, stream) != cudaSuccess) {
+    return ENGRAM_ECUDA;
+  }
   mark(c, 1, stream);
   GemmArgs a{};
   a.M = M;
   a.N = c->N;
   a.K = c->K;
   a.splits = p.splits;
-  a.kb_per_split = (c->K / kBK) / p.splits;
+  a.kb_per_split = (c->K / (c->fp8 ? 128 : kBK)) / p.splits;
   a.m_tiles = p.m_tiles;
   a.n_tiles = p.n_tiles;
   a.group_m = p.m_tiles < 16 ? p.m_tiles : 16;
@@ -165,6 +174,9 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
   a.part = c->part;
   a.err = c->err;
   a.wpack = c->wpack;
+  a.fp8 = c->fp8 ? 1 : 0;
+  a.sfa = c->sfa;
+  a.sfb = c->wsf;
   if (fuse) {
     a.out_mode = kOutFused;
     a.x = fused->x;
@@ -181,7 +193,8 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
     a.clamp = c->cfg.clamp;
     a.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c->cfg.dim)));
   }
-  if (launch_gemm(c->rows, c->tmW, a, p.ctas, stream) != cudaSuccess) return ENGRAM_ECUDA;
+  const void* rows = c->fp8 ? static_cast<const void*>(c->codes) : static_cast<const void*>(c->rows);
+  if (launch_gemm(rows, c->tmW, a, p.ctas, stream) != cudaSuccess) return ENGRAM_ECUDA;
   mark(c, 2, stream);
   *plan_out = p;
   return ENGRAM_OK;
@@ -216,6 +229,9 @@ void free_ctx(engram_ctx* c) {
   cudaFree(c->counters);
   cudaFree(c->gates);
   cudaFree(c->wpack);
+  cudaFree(c->wsf);
+  cudaFree(c->codes);
+  cudaFree(c->sfa);
   delete c;
 }
 
@@ -236,7 +252,7 @@ const char* engram_status_string(engram_status s) {
   return "unknown status";
 }
 
-int32_t engram_abi_version(void) { return 100; }
+int32_t engram_abi_version(void) { return 101; }
 
 engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w) {
   if (out == nullptr || cfg == nullptr || w == nullptr) return ENGRAM_EINVAL;
@@ -258,6 +274,13 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
   const int64_t K = static_cast<int64_t>(c.n_cols) * c.head_dim;
   const int64_t N = static_cast<int64_t>(c.dim) * (c.hc_mult + 1);
   if (K % kBK != 0 || K > (1 << 20) || N > (1 << 24)) return ENGRAM_EUNSUPPORTED;
+  if (c.wkv_fmt != ENGRAM_WKV_BF16 && c.wkv_fmt != ENGRAM_WKV_MXFP8) return ENGRAM_EUNSUPPORTED;
+  const bool fp8 = c.wkv_fmt == ENGRAM_WKV_MXFP8;
+  if (fp8) {
+    // the table's codes and scales feed the block-scaled MMA as they are
+    if (c.scale_fmt != ENGRAM_SCALE_E8M0 || c.scale_block != 32 || K % 128 != 0) return ENGRAM_EUNSUPPORTED;
+    if (w->wkv_scale == nullptr) return ENGRAM_EINVAL;
+  }
 
   engram_ctx* ctx = new (std::nothrow) engram_ctx();
   if (ctx == nullptr) return ENGRAM_ENOMEM;
@@ -265,6 +288,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
   ctx->w = *w;
   ctx->K = static_cast<int32_t>(K);
   ctx->N = static_cast<int32_t>(N);
+  ctx->fp8 = fp8;
   if (cudaGetDevice(&ctx->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
     delete ctx;
@@ -290,7 +314,12 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
             cudaMalloc(&ctx->counters, static_cast<size_t>((mt + kBM - 1) / kBM) * 8 * sizeof(uint32_t)) ==
                 cudaSuccess &&
             cudaMalloc(&ctx->gates, static_cast<size_t>(mt) * 4 * sizeof(float)) == cudaSuccess &&
-            cudaMalloc(&ctx->wpack, static_cast<size_t>(N) * K * 2) == cudaSuccess;
+            cudaMalloc(&ctx->wpack, static_cast<size_t>(N) * K * (fp8 ? 1 : 2)) == cudaSuccess;
+  const size_t sfa_bytes = static_cast<size_t>((mt + kBM - 1) / kBM) * (K / 128) * 512;
+  if (ok && fp8)
+    ok = cudaMalloc(&ctx->wsf, static_cast<size_t>(N) * (K / 32)) == cudaSuccess &&
+         cudaMalloc(&ctx->codes, static_cast<size_t>(mt) * K) == cudaSuccess &&
+         cudaMalloc(&ctx->sfa, sfa_bytes) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_ctx(ctx);
@@ -299,12 +328,15 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
   if (cudaMemset(ctx->err, 0, 2 * sizeof(unsigned long long)) != cudaSuccess ||
       launch_weight_product(w->q_weight, w->k_weight, ctx->wprod, static_cast<int64_t>(hcd), nullptr) !=
           cudaSuccess ||
-      launch_pack_wkv(w->wkv, N, K, ctx->wpack, nullptr) != cudaSuccess ||
+      (fp8 ? launch_pack_wkv(static_cast<const uint16_t*>(w->wkv), N, K / 2, ctx->wpack, nullptr) != cudaSuccess ||
+                 launch_pack_sfb(w->wkv_scale, N, K, ctx->wsf, nullptr) != cudaSuccess ||
+                 cudaMemset(ctx->sfa, 127, sfa_bytes) != cudaSuccess   // scales of rows past M: 1.0
+           : launch_pack_wkv(static_cast<const uint16_t*>(w->wkv), N, K, ctx->wpack, nullptr) != cudaSuccess) ||
       gemm_prepare() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     free_ctx(ctx);
     return ENGRAM_ECUDA;
   }
-  if (!make_tmap_bf16(&ctx->tmW, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN)) {
+  if (!fp8 && !make_tmap_bf16(&ctx->tmW, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN)) {
     free_ctx(ctx);
     return ENGRAM_ECUDA;
   }
@@ -334,7 +366,7 @@ engram_status engram_forward(engram_ctx* ctx, const int64_t* hash_ids, const uin
   const FusedIO io{x, token_mask, out};
   st = run_projection(ctx, hash_ids, M, ctx->kv, &io, &p, s);
   if (st != ENGRAM_OK) return st;
-  if (ctx->cfg.fuse_gate && fuses(p, M)) {   // the projection's epilogue applied the gate
+  if (ctx->cfg.fuse_gate && fuses(ctx, p, M)) {   // the projection's epilogue applied the gate
     mark(ctx, 3, s);
     return ENGRAM_OK;
   }

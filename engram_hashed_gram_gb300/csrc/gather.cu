@@ -79,7 +79,58 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
   }
 }
 
+// One thread per 16-byte chunk of a row's codes; the first head_dim/32
+// threads of a row also place its scales.
+__global__ void __launch_bounds__(256) gather_codes_kernel(GatherArgs a, int n_cols, int64_t kbt,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ sfa) {
+  grid_dependency_wait();        // the ids may come from the previous kernel
+  grid_launch_dependents();      // let the projection start its weight stream
+  if (a.zero != nullptr) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero; i += gridDim.x * blockDim.x) a.zero[i] = 0u;
+  }
+  const int cpr = a.head_dim >> 4;
+  const int nb = a.head_dim >> 5;
+  const int64_t K = static_cast<int64_t>(n_cols) * a.head_dim;
+  const int64_t total = a.rows_total * cpr;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t row = i / cpr;
+    const int ch = static_cast<int>(i - row * cpr);
+    const int64_t m = row / n_cols;
+    const int c = static_cast<int>(row - m * n_cols);
+    const int64_t r = __ldg(a.ids + row);
+    const bool valid = r >= 0 && r < a.R;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) {
+      v = ld_stream_v4(a.table + r * a.head_dim + ch * 16);
+    } else if (a.check_ids && ch == 0) {
+      atomicAdd(a.err + 1, 1ull);
+      atomicOr(a.err, kErrRange);
+    }
+    *reinterpret_cast<uint4*>(codes + m * K + static_cast<int64_t>(c) * a.head_dim + ch * 16) = v;
+    if (ch < nb) {
+      const uint8_t sc = valid ? __ldg(static_cast<const uint8_t*>(a.scale) + r * nb + ch) : uint8_t{127};
+      const int64_t q = (static_cast<int64_t>(c) * a.head_dim >> 5) + ch;   // K-block of 32
+      const int t = static_cast<int>(m & 127);
+      sfa[(((m >> 7) * kbt + (q >> 2)) << 9) + ((t & 31) << 4) + ((t >> 5) << 2) + (q & 3)] = sc;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_codes(const GatherArgs& a, int n_cols, uint8_t* codes, uint8_t* sfa, int num_sms,
+                                cudaStream_t stream) {
+  const int64_t total = a.rows_total * (a.head_dim >> 4);
+  if (total == 0) return cudaSuccess;
+  const int64_t K = static_cast<int64_t>(n_cols) * a.head_dim;
+  if (K % 128 != 0 || a.head_dim % 32 != 0) return cudaErrorInvalidValue;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(gather_codes_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, a, n_cols,
+                    K / 128, codes, sfa);
+}
 
 cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream) {
   const int64_t total = a.rows_total * (a.head_dim >> 4);

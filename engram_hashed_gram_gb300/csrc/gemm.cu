@@ -23,6 +23,17 @@
 // whatever the neighbouring shared memory holds, their accumulator rows are
 // never stored, and a row of D depends on its own row of A only.  Rows of the
 // last M tile past M read as zeros (TMA bounds fill) and are not stored.
+//
+// MXFP8 weight (FP8 = true): A is the gathered table codes (e4m3, [M, K]) and
+// B the weight's codes, each with one E8M0 scale per 32 K per row; a stage is
+// K = 128 (still 128 bytes per row), plus the stage's scales: 512 bytes for
+// the 128 rows of A and 1 KB for the 256 rows of B, each a 32-line x 16-byte
+// block in which line l holds the 4 scales (one per 32 K) of rows l, l+32,
+// l+64, l+96.  The MMA thread copies them into tensor memory (tcgen05.cp,
+// 32x128b replicated to the four lane quarters) and issues four
+// tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each; the instruction
+// descriptor picks the scale byte).  The accumulator is single-buffered: the
+// scales take tensor-memory columns 256 and up.
 #include <algorithm>
 #include <mutex>
 
@@ -33,7 +44,12 @@ namespace engram {
 namespace {
 
 constexpr int kBBytes = kBN * kBK * 2;        // 32 KB
-constexpr uint32_t kTmemCols = 2 * kBN;        // two fp32 accumulators
+constexpr uint32_t kTmemCols = 2 * kBN;        // two fp32 accumulators (bf16), or one + scales (FP8)
+constexpr int kKB8 = 128;                      // K elements per FP8 stage (128 bytes per row)
+constexpr int kSfaBytes = 512;                 // scales of 128 A rows x 4 K-blocks of 32
+constexpr int kSfbBytes = 1024;                // scales of 256 B rows x 4
+constexpr uint32_t kSfCol0 = kBN;              // first tensor-memory column of the FP8 scales
+constexpr uint32_t kSfColsPerStage = 16;       // A: 4 columns, B: 8 columns
 
 constexpr int kMaxStreams = 4;                 // hc_mult
 constexpr int kMaxBlocks = 5120 / kBN;         // 256-channel blocks per stream (dim <= 5120)
@@ -46,16 +62,20 @@ constexpr int kEpiGates = 32 * kEpiPitch;            // float [32][4]
 constexpr int kEpiFlags = kEpiGates + 32 * 16;       // int [32]
 constexpr int kEpiWarpBytes = kEpiFlags + 32 * 4;    // 3,200
 
-template <int A_ROWS, int STAGES>
+template <int A_ROWS, int STAGES, bool FP8 = false>
 struct Cfg {
-  static constexpr int kABytes = A_ROWS * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kABytes = A_ROWS * kBK * 2;                  // A_ROWS x 128 bytes either way
+  static constexpr int kSfBytes = FP8 ? kSfaBytes + kSfbBytes : 0;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;  // bytes one stage's copies deliver
+  static constexpr int kSfOffset = STAGES * (kABytes + kBBytes);
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
   static constexpr int kEpiOffset = kBarOffset + 256;              // fused-mode staging, after the barriers
   static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kEpiOffset;
   static constexpr size_t kSmemFused = kSmemBytes + 4 * kEpiWarpBytes;
-  static constexpr bool kCanFuse = kSmemFused <= 232448;
+  static constexpr bool kCanFuse = !FP8 && kSmemFused <= 232448;
+  static_assert(!kCanFuse || kSmemFused <= 232448, "fused-mode shared memory");
+  static_assert(!FP8 || STAGES * kSfColsPerStage + kSfCol0 <= kTmemCols, "scale columns");
   static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
   static_assert(kABytes % 1024 == 0, "A stages must stay 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -97,13 +117,33 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& m
 
 // The weight tile (N tile nt, K block kb) into a B stage: one contiguous 32 KB
 // copy from the packed weight, or a 2-D tensor copy of the row-major weight.
-__device__ __forceinline__ void load_b(const GemmArgs& a, const CUtensorMap& tmB, uint8_t* dst, uint64_t* bar, int nt,
-                                       int kb, uint64_t policy) {
-  if (a.wpack != nullptr) {
-    const int64_t tile = static_cast<int64_t>(nt) * (a.K / kBK) + kb;
+// FP8: the tile's scales (1 KB, packed the same way) go to the stage's B-scale
+// block.  kbt = K blocks per row of tiles.
+template <bool FP8>
+__device__ __forceinline__ void load_b(const GemmArgs& a, const CUtensorMap& tmB, uint8_t* dst, uint8_t* sf_dst,
+                                       uint64_t* bar, int nt, int kb, int kbt, uint64_t policy) {
+  const int64_t tile = static_cast<int64_t>(nt) * kbt + kb;
+  if constexpr (FP8) {
+    bulk_load_hint(dst, a.wpack + tile * kBBytes, kBBytes, bar, policy);
+    bulk_load_hint(sf_dst + kSfaBytes, a.sfb + tile * kSfbBytes, kSfbBytes, bar, policy);
+  } else if (a.wpack != nullptr) {
     bulk_load_hint(dst, a.wpack + tile * kBBytes, kBBytes, bar, policy);
   } else {
     tma_load_2d_hint(dst, &tmB, bar, kb * kBK, nt * kBN, policy);
+  }
+}
+
+// The gathered rows (M tile mt, K block kb) into an A stage; FP8: with their
+// scales (512 bytes, from the gather) into the stage's A-scale block.
+template <bool FP8>
+__device__ __forceinline__ void load_a(const GemmArgs& a, const CUtensorMap& tmA, uint8_t* dst, uint8_t* sf_dst,
+                                       uint64_t* bar, int mt, int kb, int kbt) {
+  if constexpr (FP8) {
+    tma_load_2d(dst, &tmA, bar, kb * kKB8, mt * kBM);
+    bulk_load_hint(sf_dst, a.sfa + (static_cast<int64_t>(mt) * kbt + kb) * kSfaBytes, kSfaBytes, bar,
+                   policy_evict_last());
+  } else {
+    tma_load_2d(dst, &tmA, bar, kb * kBK, mt * kBM);
   }
 }
 
@@ -364,12 +404,14 @@ __device__ __forceinline__ bool fused_value_epilogue(const GemmArgs& a, uint32_t
 }
 
 // FUSED selects the gate epilogue at compile time, so that the plain kernel
-// carries none of its registers.
-template <int A_ROWS, int STAGES, bool FUSED>
+// carries none of its registers; FP8 the block-scaled MXFP8 operands.
+template <int A_ROWS, int STAGES, bool FUSED, bool FP8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
-  using C = Cfg<A_ROWS, STAGES>;
+  static_assert(!(FUSED && FP8), "the fused epilogue takes bf16 weights only");
+  using C = Cfg<A_ROWS, STAGES, FP8>;
+  constexpr int kAccBufs = FP8 ? 1 : 2;
   constexpr int kStages = STAGES;
   constexpr int kABytes = C::kABytes;
   constexpr int kStageBytes = C::kStageBytes;
@@ -378,6 +420,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smem + kStages * kABytes;
+  uint8_t* smSF = smem + C::kSfOffset;             // FP8: per stage, A scales then B scales
+  const int kbt = a.K / (FP8 ? kKB8 : kBK);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
@@ -432,7 +476,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         pre = min(kStages, a.kb_per_split);
         for (int i = 0; i < pre; ++i) {   // fresh ring: every stage is free
           mbar_arrive_expect_tx(&full[i], kStageBytes);
-          load_b(a, tmB, smB + i * kBBytes, &full[i], nt, sp * a.kb_per_split + i, pol_w);
+          load_b<FP8>(a, tmB, smB + i * kBBytes, smSF + i * C::kSfBytes, &full[i], nt, sp * a.kb_per_split + i,
+                      kbt, pol_w);
         }
       }
       grid_dependency_wait();     // the gathered rows are written by the gather kernel
@@ -444,17 +489,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         unit_coords<FUSED>(a, u, mt, nt, sp);
         const int kb0 = sp * a.kb_per_split;
         for (int kb = 0; kb < a.kb_per_split; ++kb) {
+          uint8_t* sf = smSF + stage * C::kSfBytes;
           if (u == blockIdx.x && kb < pre) {
             // weight tile already in flight on this stage: add the rows
-            tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], (kb0 + kb) * kBK, mt * kBM);
+            load_a<FP8>(a, tmA, smA + stage * kABytes, sf, &full[stage], mt, kb0 + kb, kbt);
           } else {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(&full[stage], kStageBytes);
-            tma_load_2d(smA + stage * kABytes, &tmA, &full[stage], (kb0 + kb) * kBK, mt * kBM);
-            load_b(a, tmB, smB + stage * kBBytes, &full[stage], nt, kb0 + kb, pol_w);
+            load_a<FP8>(a, tmA, smA + stage * kABytes, sf, &full[stage], mt, kb0 + kb, kbt);
+            load_b<FP8>(a, tmB, smB + stage * kBBytes, sf, &full[stage], nt, kb0 + kb, kbt, pol_w);
           }
           ++issued[stage];
           if (++stage == kStages) {
@@ -497,10 +543,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smA + stage * kABytes));
           const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smB + stage * kBBytes));
+          if constexpr (FP8) {
+            // the stage's scales into tensor memory, then four K = 32 steps
+            // (+32 bytes each) that take scale byte kk of each 32-bit column
+            const uint32_t sf_col = tmem_base + kSfCol0 + static_cast<uint32_t>(stage) * kSfColsPerStage;
+            const uint32_t sf_smem = smem_u32(smSF + stage * C::kSfBytes);
+            tmem_cp_32x128b_warpx4(sf_col, sdesc_rows16(sf_smem));
+            tmem_cp_32x128b_warpx4(sf_col + 4, sdesc_rows16(sf_smem + kSfaBytes));
+            tmem_cp_32x128b_warpx4(sf_col + 8, sdesc_rows16(sf_smem + kSfaBytes + kSfbBytes / 2));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // +32 bytes per K step of 16 bf16 = +2 in the start-address field
-            umma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              umma_mxf8(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc_mxf8_e4m3(kBM, kBN, kk), sf_col,
+                        sf_col + 4, (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // +32 bytes per K step of 16 bf16 = +2 in the start-address field
+              umma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -510,8 +571,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // every MMA issued by this thread completes before the tensor memory is freed
       umma_commit(drain);
@@ -550,8 +613,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
     if (!ok && lane == 0) raise_abort(abort_flag, a.err);
     __syncwarp();
@@ -566,11 +631,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int A_ROWS, int STAGES>
 cudaError_t set_smem_attr() {
   using C = Cfg<A_ROWS, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, false>,
+  using C8 = Cfg<A_ROWS, STAGES, true>;
+  cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
   if (e == cudaSuccess && C::kCanFuse)
-    e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::kSmemFused));
+    e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemFused));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C8::kSmemBytes));
   return e;
 }
 
@@ -579,12 +648,17 @@ cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            cudaStream_t stream) {
   using C = Cfg<A_ROWS, STAGES>;
   const bool fused = a.out_mode == kOutFused;
+  if (a.fp8) {
+    if (fused || a.wpack == nullptr || a.sfa == nullptr || a.sfb == nullptr) return cudaErrorInvalidConfiguration;
+    return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, false, true>, dim3(static_cast<unsigned>(ctas)),
+                      dim3(kGemmThreads), Cfg<A_ROWS, STAGES, true>::kSmemBytes, stream, 1, tmA, tmB, a);
+  }
   if (!fused)
-    return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, false>, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads),
-                      C::kSmemBytes, stream, 1, tmA, tmB, a);
+    return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, false, false>, dim3(static_cast<unsigned>(ctas)),
+                      dim3(kGemmThreads), C::kSmemBytes, stream, 1, tmA, tmB, a);
   if (!C::kCanFuse) return cudaErrorInvalidConfiguration;
-  return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, true>, dim3(static_cast<unsigned>(ctas)), dim3(kGemmThreads),
-                    C::kSmemFused, stream, 1, tmA, tmB, a);
+  return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, true, false>, dim3(static_cast<unsigned>(ctas)),
+                    dim3(kGemmThreads), C::kSmemFused, stream, 1, tmA, tmB, a);
 }
 
 // One thread per 16-byte chunk of the packed weight: chunk p of row r of a tile
@@ -601,6 +675,27 @@ __global__ void __launch_bounds__(256) pack_wkv_kernel(const uint16_t* __restric
     const int64_t kb = tile - nt * kb_total;
     const int64_t n = nt * kBN + r;
     out[i] = __ldg(reinterpret_cast<const uint4*>(w + n * K + kb * kBK + c * 8));
+  }
+}
+
+// One thread per byte of the packed FP8 weight scales: tile (n_tile, k_block)
+// holds 1 KB, two 512-byte blocks (rows 0-127, 128-255 of the tile); in a
+// block, byte 16*l + 4*q + j is the scale of K-block j of row l + 32*q.
+__global__ void __launch_bounds__(256) pack_sfb_kernel(const uint8_t* __restrict__ sc, int64_t kb_total,
+                                                       int64_t bytes, uint8_t* __restrict__ out) {
+  const int64_t per_row = kb_total * 4;               // scales per weight row (K / 32)
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < bytes;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tile = i >> 10;
+    const int b = static_cast<int>(i & 1023);
+    const int half = b >> 9;
+    const int l = (b >> 4) & 31;
+    const int q = (b >> 2) & 3;
+    const int j = b & 3;
+    const int64_t nt = tile / kb_total;
+    const int64_t kb = tile - nt * kb_total;
+    const int64_t n = nt * kBN + half * 128 + q * 32 + l;
+    out[i] = sc[n * per_row + kb * 4 + j];
   }
 }
 
@@ -639,6 +734,18 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKB8), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t gemm_prepare() {
   cudaError_t e = set_smem_attr<128, 4>();
   if (e == cudaSuccess) e = set_smem_attr<64, 5>();
@@ -655,13 +762,25 @@ cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const uint16_t* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
+cudaError_t launch_pack_sfb(const uint8_t* wkv_scale, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream) {
+  if (N % kBN != 0 || K % kKB8 != 0) return cudaErrorInvalidValue;
+  const int64_t bytes = N * K / 32;
+  if (bytes == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((bytes + 255) / 256, 65536);
+  pack_sfb_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(wkv_scale, K / kKB8, bytes, packed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const void* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
                         cudaStream_t stream) {
   if (a.units == 0) return cudaSuccess;
   const int ar = gemm_a_rows(a.M);
   CUtensorMap tmA;
-  if (!make_tmap_bf16(&tmA, rows, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), static_cast<uint32_t>(ar)))
-    return cudaErrorInvalidValue;
+  const bool mapped =
+      a.fp8 ? make_tmap_u8(&tmA, rows, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), static_cast<uint32_t>(ar))
+            : make_tmap_bf16(&tmA, rows, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K),
+                             static_cast<uint32_t>(ar));
+  if (!mapped) return cudaErrorInvalidValue;
   if (ar == 32) return launch_variant<32, 6>(tmA, tmB, a, ctas, stream);
   if (ar == 64) return launch_variant<64, 5>(tmA, tmB, a, ctas, stream);
   return launch_variant<128, 4>(tmA, tmB, a, ctas, stream);

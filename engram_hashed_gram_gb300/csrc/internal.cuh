@@ -56,6 +56,15 @@ struct GatherArgs {
   int32_t n_zero;
 };
 cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
+// MXFP8 operands for the block-scaled projection: the rows' e4m3 codes copied
+// to codes [M, K] (a zero row for an id outside [0, R)) and their E8M0 scales
+// (scale_block 32) to sfa in the projection's A-scale order: 512 bytes per
+// (M tile of 128, K block of 128) at byte (m_tile * K/128 + k_block) * 512,
+// byte 16*l + 4*q + j = scale of K-block j (of 32) of row l + 32*q of the tile
+// (127, i.e. 1.0, for a zero row).  Uses ids, table, scale, rows_total, R,
+// head_dim, check_ids, err, zero/n_zero of `a`.
+cudaError_t launch_gather_codes(const GatherArgs& a, int n_cols, uint8_t* codes, uint8_t* sfa, int num_sms,
+                                cudaStream_t stream);
 
 // ---- projection (step a4) --------------------------------------------------
 constexpr int kBM = 128;     // tokens per tile (MMA M)
@@ -77,6 +86,9 @@ struct GemmArgs {
   int64_t units;         // m_tiles * n_tiles * splits
   int32_t out_mode;      // GemmOut
   const uint8_t* wpack;  // the weight in tile-packed order (pack_wkv), or nullptr: read through tmB
+  int32_t fp8;           // MXFP8 operands: A = table codes [M, K] u8, B = packed weight codes
+  const uint8_t* sfa;    // fp8: A scales, [m_tiles, K/128, 512] (gather_codes layout)
+  const uint8_t* sfb;    // fp8: B scales, [n_tiles, K/128, 1024] (pack_sfb layout)
   uint16_t* kv;          // kOutBf16: [M, N]
   float* part;           // kOutPartial: [splits, M, N]
   unsigned long long* err;
@@ -102,9 +114,10 @@ int gemm_a_rows(int64_t M);
 bool gemm_can_fuse(int64_t M);
 // bf16 [rows, cols] row-major matrix, box = [box_rows, 64 columns], 128-byte swizzle.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
-// rows: the gathered rows [M, K] (its tensor map is built here, to match the
-// kernel variant); tmB: the weight's map, box [256 rows, 64 columns].
-cudaError_t launch_gemm(const uint16_t* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
+// rows: the gathered rows [M, K], bf16 or (fp8) e4m3 codes (its tensor map is
+// built here, to match the kernel variant); tmB: the weight's map, box [256
+// rows, 64 columns] (unused when a.wpack is set).
+cudaError_t launch_gemm(const void* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
                         cudaStream_t stream);
 // The weight [N, K] (N a multiple of 256, K of 64) rewritten as 32 KB tiles,
 // tile (n_tile, k_block) at byte offset (n_tile * K/64 + k_block) * 32768, each
@@ -112,6 +125,13 @@ cudaError_t launch_gemm(const uint16_t* rows, const CUtensorMap& tmB, const Gemm
 // 128-byte-swizzled tensor copy of that box lands in shared memory.  `packed`
 // holds N*K*2 bytes, 16-byte aligned.
 cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream);
+// The MXFP8 weight's E8M0 scales [N, K/32] in the projection's order: 1 KB per
+// (n_tile, k_block of 128) at byte (n_tile * K/128 + k_block) * 1024; rows
+// 0-127 of the tile in the first 512 bytes, 128-255 in the second; in each,
+// byte 16*l + 4*q + j = scale of K-block j (of 32) of row l + 32*q.  The
+// codes themselves are packed by launch_pack_wkv viewing [N, K] bytes as
+// [N, K/2] 16-bit elements.
+cudaError_t launch_pack_sfb(const uint8_t* wkv_scale, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream);
 
 // ---- gate and residual (steps a5-a8) ---------------------------------------
 struct GateArgs {

@@ -78,6 +78,7 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
       !(c.eps >= 0.0f) || !(c.clamp >= 0.0f))
     return ENGRAM_EINVAL;
   if (c.scale_fmt != ENGRAM_SCALE_F32 && c.scale_fmt != ENGRAM_SCALE_E8M0) return ENGRAM_EUNSUPPORTED;
+  if (c.wkv_fmt != ENGRAM_WKV_BF16) return ENGRAM_EUNSUPPORTED;   // the MXFP8 weight needs a context's packed copy
   if (c.dim % kBN != 0 || c.dim > 5120 || c.hc_mult > 4 || c.head_dim % 16 != 0 || c.head_dim % c.scale_block != 0 ||
       c.scale_block % 16 != 0)
     return ENGRAM_EUNSUPPORTED;

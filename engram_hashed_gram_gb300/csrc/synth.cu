@@ -59,7 +59,32 @@ __global__ void fill_scales_kernel(float* __restrict__ scale, int64_t row_begin,
   }
 }
 
+__global__ void fill_scales_e8m0_kernel(uint8_t* __restrict__ scale, int64_t row_begin, int64_t row_end, int nb,
+                                        uint64_t key, const uint8_t* __restrict__ qtable) {
+  const int64_t total = (row_end - row_begin) * nb;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint64_t c = static_cast<uint64_t>(row_begin) * nb + static_cast<uint64_t>(i);
+    scale[c] = __ldg(qtable + (draw(key, c) >> 48));
+  }
+}
+
 }  // namespace
+
+extern "C" int32_t engram_synth_fill_scales_e8m0(uint8_t* scale, int64_t row_begin, int64_t row_end,
+                                                 int32_t head_dim, int32_t scale_block, uint64_t key_scales,
+                                                 const uint8_t* e8m0_qtable, engram_synth_stream_t stream) {
+  if (scale == nullptr || e8m0_qtable == nullptr || row_begin < 0 || row_end < row_begin || head_dim <= 0 ||
+      scale_block <= 0 || head_dim % scale_block != 0)
+    return -1;
+  if (row_end == row_begin) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -3;
+  fill_scales_e8m0_kernel<<<sms * 4, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      scale, row_begin, row_end, head_dim / scale_block, key_scales, e8m0_qtable);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
 
 extern "C" int32_t engram_synth_fill_table(uint8_t* table, float* scale, int64_t row_begin, int64_t row_end,
                                            int32_t head_dim, int32_t scale_block, uint64_t key_codes,

@@ -47,12 +47,14 @@ class EngramLayer:
 
     table: uint8 [R, head_dim] e4m3 codes; scale: float32 [R, head_dim/scale_block]
     (or uint8 E8M0 codes with scale_fmt=SCALE_E8M0); wkv: bf16 [dim*(hc+1),
-    n_cols*head_dim]; q_weight, k_weight: bf16 [hc, dim].  The tensors are
-    referenced, not copied, and are kept alive by this object."""
+    n_cols*head_dim], or its uint8 e4m3 codes together with wkv_scale (uint8
+    E8M0 [dim*(hc+1), n_cols*head_dim/32]) for the MXFP8 weight; q_weight,
+    k_weight: bf16 [hc, dim].  The tensors are referenced, not copied, and are
+    kept alive by this object."""
 
     def __init__(self, table, scale, wkv, q_weight, k_weight, *, dim=5120, hc_mult=4, n_cols=24, head_dim=256,
                  scale_block=128, scale_fmt=_lib.SCALE_F32, eps=1e-6, clamp=1e-6, max_tokens=4096,
-                 check_ids=False, fuse_gate=False):
+                 check_ids=False, fuse_gate=False, wkv_scale=None):
         dev = table.device
         if dev.type != "cuda":
             raise ValueError("the Engram layer runs on a CUDA device only")
@@ -60,7 +62,12 @@ class EngramLayer:
         _need(table, "table", (torch.uint8,), (R, head_dim), dev)
         _need(scale, "scale", (torch.float32,) if scale_fmt == _lib.SCALE_F32 else (torch.uint8,),
               (R, head_dim // scale_block), dev)
-        _need(wkv, "wkv", _U16, (dim * (hc_mult + 1), n_cols * head_dim), dev)
+        wkv_fmt = _lib.WKV_BF16 if wkv_scale is None else _lib.WKV_MXFP8
+        if wkv_fmt == _lib.WKV_BF16:
+            _need(wkv, "wkv", _U16, (dim * (hc_mult + 1), n_cols * head_dim), dev)
+        else:
+            _need(wkv, "wkv", (torch.uint8,), (dim * (hc_mult + 1), n_cols * head_dim), dev)
+            _need(wkv_scale, "wkv_scale", (torch.uint8,), (dim * (hc_mult + 1), n_cols * head_dim // 32), dev)
         _need(q_weight, "q_weight", _U16, (hc_mult, dim), dev)
         _need(k_weight, "k_weight", _U16, (hc_mult, dim), dev)
         self.device = dev
@@ -68,13 +75,13 @@ class EngramLayer:
         self.N = dim * (hc_mult + 1)
         self.K = n_cols * head_dim
         self.max_tokens = max_tokens
-        self._keep = (table, scale, wkv, q_weight, k_weight)
+        self._keep = (table, scale, wkv, q_weight, k_weight, wkv_scale)
         self.cfg = EngramConfig(dim=dim, hc_mult=hc_mult, n_cols=n_cols, head_dim=head_dim,
                                 scale_block=scale_block, scale_fmt=scale_fmt, num_rows=R, eps=eps, clamp=clamp,
                                 max_tokens=max_tokens, check_ids=1 if check_ids else 0,
-                                fuse_gate=1 if fuse_gate else 0)
+                                fuse_gate=1 if fuse_gate else 0, wkv_fmt=wkv_fmt)
         w = EngramWeights(table=_ptr(table), scale=_ptr(scale), wkv=_ptr(wkv), q_weight=_ptr(q_weight),
-                          k_weight=_ptr(k_weight))
+                          k_weight=_ptr(k_weight), wkv_scale=_ptr(wkv_scale))
         self._ctx = ctypes.c_void_p()
         self._lib = _lib.engram()
         with torch.cuda.device(dev):

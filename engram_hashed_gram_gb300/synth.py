@@ -54,6 +54,8 @@ MIX2 = 0x94D049BB133111EB
 
 TAG_CODES = 1
 TAG_SCALES = 2
+TAG_WKV_CODES = 3
+TAG_WKV_SCALES = 4
 
 
 # --------------------------------------------------------------------------
@@ -152,12 +154,22 @@ def scale_quantile_table() -> np.ndarray:
     return _QT_CACHE["scales"]
 
 
+def e8m0_quantile_table() -> np.ndarray:
+    """uint8[65536]: E8M0 code of the power of two nearest (in log2) to the
+    lognormal(0, 0.5) quantile at (u+0.5)/65536: 127 + round(log2 q)."""
+    if "e8m0" not in _QT_CACHE:
+        q = scale_quantile_table().astype(np.float64)
+        _QT_CACHE["e8m0"] = np.clip(127 + np.rint(np.log2(q)), 1, 254).astype(np.uint8)
+    return _QT_CACHE["e8m0"]
+
+
 # --------------------------------------------------------------------------
 # table rows (host twin of the device filler)
 # --------------------------------------------------------------------------
-def table_rows(seed: int, rows: np.ndarray, head_dim: int = 256, scale_block: int = 128):
-    """Codes (uint8 [n, head_dim]) and fp32 scales ([n, head_dim/scale_block])
-    of the given table rows, exactly as the device filler writes them."""
+def table_rows(seed: int, rows: np.ndarray, head_dim: int = 256, scale_block: int = 128, scale_fmt: int = 0):
+    """Codes (uint8 [n, head_dim]) and scales ([n, head_dim/scale_block]: fp32,
+    or E8M0 bytes when scale_fmt == 1, drawn at the same stream positions) of
+    the given table rows, exactly as the device filler writes them."""
     rows = np.asarray(rows, dtype=np.int64).reshape(-1)
     assert head_dim % 4 == 0 and head_dim % scale_block == 0
     words = head_dim // 4
@@ -172,17 +184,20 @@ def table_rows(seed: int, rows: np.ndarray, head_dim: int = 256, scale_block: in
     codes = ctab[fields.astype(np.int64)].reshape(rows.size, head_dim)
     scnt = rows.astype(np.uint64)[:, None] * np.uint64(nb) + np.arange(nb, dtype=np.uint64)[None, :]
     sidx = (draw64(ks, scnt) >> np.uint64(48)).astype(np.int64)
+    if scale_fmt == 1:
+        return codes.astype(np.uint8), e8m0_quantile_table()[sidx]
     scales = stab[sidx].astype(np.float32)
     return codes.astype(np.uint8), scales
 
 
-def host_table(seed: int, num_rows: int, head_dim: int = 256, scale_block: int = 128, chunk: int = 1 << 16):
+def host_table(seed: int, num_rows: int, head_dim: int = 256, scale_block: int = 128, chunk: int = 1 << 16,
+               scale_fmt: int = 0):
     """The whole table on the host (small tables only)."""
     codes = np.empty((num_rows, head_dim), dtype=np.uint8)
-    scales = np.empty((num_rows, head_dim // scale_block), dtype=np.float32)
+    scales = np.empty((num_rows, head_dim // scale_block), dtype=np.uint8 if scale_fmt == 1 else np.float32)
     for s in range(0, num_rows, chunk):
         e = min(num_rows, s + chunk)
-        c, sc = table_rows(seed, np.arange(s, e), head_dim, scale_block)
+        c, sc = table_rows(seed, np.arange(s, e), head_dim, scale_block, scale_fmt)
         codes[s:e] = c
         scales[s:e] = sc
     return codes, scales
@@ -221,6 +236,15 @@ class Workload:
     eps: float = 1e-6
     zipf_s: float = 1.1
     hot_rows: int = 1024
+    fmt: str = "bf16"             # bf16: fp32 scales + bf16 wkv | mxfp8: E8M0/32 scales + FP8 wkv
+
+    @property
+    def scale_fmt(self) -> int:
+        return 1 if self.fmt == "mxfp8" else 0
+
+    @property
+    def wkv_fmt(self) -> int:
+        return 1 if self.fmt == "mxfp8" else 0
 
     @property
     def M(self) -> int:
@@ -248,6 +272,10 @@ WORKLOADS = [
     Workload("decode_512x1_skew", 512, 1, 1 << 22, ids="hotset", x_std=math.sqrt(2.0),
              x_tiny_frac=0.01, seed=3),
     Workload("full_2x8192", 2, 8192, 16_000_000, prime_skip=24, mask="frac5", seed=4),
+    # the V4.1-native formats: MXFP8 table (E8M0 per 32) and FP8 weight
+    Workload("tiny_1x16_mxfp8", 1, 16, 4096, seed=5, scale_block=32, fmt="mxfp8"),
+    Workload("decode_64x1_mxfp8", 64, 1, 1 << 20, seed=6, scale_block=32, fmt="mxfp8"),
+    Workload("prefill_1x4096_mxfp8", 1, 4096, 1 << 22, mask="span10", seed=7, scale_block=32, fmt="mxfp8"),
 ]
 
 
@@ -333,6 +361,31 @@ def make_wkv(w: Workload, rng=None) -> np.ndarray:
     return to_bf16_bits(a)
 
 
+def make_wkv_mxfp8(w: Workload, rows_per_chunk: int = 1024):
+    """FP8 weight: (e4m3 codes uint8 [N, K], E8M0 scales uint8 [N, K/32]).
+    Codes are N(0,1) quantiles (the table's code quantile table) drawn from a
+    counter stream, 4 codes per draw like the table; each 32-input block gets
+    the scale 2^-7 or 2^-6 from the top bit of a second stream, so that the
+    entries have about the bf16 weight's spread, N(0, 1/K)."""
+    N, K = w.N, w.K
+    assert K % 32 == 0
+    ctab = code_quantile_table()
+    kc = stream_key(w.seed, TAG_WKV_CODES)
+    ks = stream_key(w.seed, TAG_WKV_SCALES)
+    words = K // 4
+    codes = np.empty((N, K), dtype=np.uint8)
+    for j0 in range(0, N, rows_per_chunk):
+        j1 = min(N, j0 + rows_per_chunk)
+        cnt = np.arange(j0, j1, dtype=np.uint64)[:, None] * np.uint64(words) + np.arange(words, dtype=np.uint64)[None, :]
+        d = draw64(kc, cnt)
+        f = np.stack([(d >> np.uint64(16 * q)) & np.uint64(0xFFFF) for q in range(4)], axis=-1)
+        codes[j0:j1] = ctab[f.astype(np.int64)].reshape(j1 - j0, K)
+    nb = K // 32
+    top = draw64(ks, np.arange(N * nb, dtype=np.uint64)) >> np.uint64(63)
+    scales = (np.uint64(120) + top).astype(np.uint8).reshape(N, nb)
+    return codes, scales
+
+
 def make_qk(w: Workload, rng=None):
     """bf16 bits q_weight, k_weight [hc_mult, dim], entries 1 + N(0, 0.1)."""
     rng = rng or np.random.default_rng([w.seed, 15])
@@ -349,16 +402,22 @@ class HostInputs:
     hash_ids: np.ndarray
     x: np.ndarray
     mask: np.ndarray | None
-    wkv: np.ndarray
+    wkv: np.ndarray               # bf16 bits, or e4m3 codes for the mxfp8 format
     q: np.ndarray
     k: np.ndarray
     lengths: np.ndarray = field(default=None)
     offsets: np.ndarray = field(default=None)
+    wkv_scale: np.ndarray | None = None   # E8M0 [N, K/32] for the mxfp8 format
 
 
 def make_inputs(w: Workload) -> HostInputs:
     lengths, offsets = w.layout()
     q, k = make_qk(w)
+    wkv_scale = None
+    if w.fmt == "mxfp8":
+        wkv, wkv_scale = make_wkv_mxfp8(w)
+    else:
+        wkv = make_wkv(w)
     return HostInputs(w=w, hash_ids=make_hash_ids(w, lengths, offsets), x=make_x(w),
-                      mask=make_mask(w), wkv=make_wkv(w), q=q, k=k,
-                      lengths=lengths, offsets=offsets)
+                      mask=make_mask(w), wkv=wkv, q=q, k=k,
+                      lengths=lengths, offsets=offsets, wkv_scale=wkv_scale)

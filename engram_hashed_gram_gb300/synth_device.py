@@ -35,12 +35,33 @@ def fill_table(table: torch.Tensor, scale: torch.Tensor | None, seed: int, scale
     torch.cuda.current_stream(dev).synchronize()
 
 
+def fill_scales_e8m0(scale: torch.Tensor, seed: int, head_dim: int, scale_block: int, stream=None) -> None:
+    """Writes the E8M0 scales (uint8 [R, head_dim/scale_block]) exactly as
+    synth.table_rows(seed, ..., scale_fmt=1)."""
+    lib = _lib.synth()
+    R = scale.shape[0]
+    dev = scale.device
+    eq = torch.from_numpy(synth.e8m0_quantile_table().copy()).to(dev)
+    st = torch.cuda.current_stream(dev).cuda_stream if stream is None else int(stream)
+    _check(lib.engram_synth_fill_scales_e8m0(scale.data_ptr(), 0, R, head_dim, scale_block,
+                                             synth.stream_key(seed, synth.TAG_SCALES), eq.data_ptr(), st),
+           "engram_synth_fill_scales_e8m0")
+    torch.cuda.current_stream(dev).synchronize()
+
+
 def make_table(w: synth.Workload, device="cuda", num_rows: int | None = None):
-    """(table uint8 [R, head_dim], scale fp32 [R, head_dim/scale_block]) on the device."""
+    """(table uint8 [R, head_dim], scales [R, head_dim/scale_block]) on the
+    device: fp32 scales, or E8M0 bytes for the mxfp8 format."""
     R = w.num_rows() if num_rows is None else num_rows
     table = torch.empty((R, w.head_dim), dtype=torch.uint8, device=device)
-    scale = torch.empty((R, w.head_dim // w.scale_block), dtype=torch.float32, device=device)
-    fill_table(table, scale, w.seed, w.scale_block)
+    nb = w.head_dim // w.scale_block
+    if w.scale_fmt == 1:
+        fill_table(table, None, w.seed, w.scale_block)
+        scale = torch.empty((R, nb), dtype=torch.uint8, device=device)
+        fill_scales_e8m0(scale, w.seed, w.head_dim, w.scale_block)
+    else:
+        scale = torch.empty((R, nb), dtype=torch.float32, device=device)
+        fill_table(table, scale, w.seed, w.scale_block)
     return table, scale
 
 
@@ -56,12 +77,15 @@ def device_bits(t: torch.Tensor) -> np.ndarray:
 
 
 def upload_inputs(inp: synth.HostInputs, device="cuda"):
-    """dict of device tensors: hash_ids, x, mask, wkv, q, k."""
+    """dict of device tensors: hash_ids, x, mask, wkv, q, k, wkv_scale (None
+    for a bf16 weight; for the mxfp8 format wkv holds the uint8 codes)."""
+    fp8 = inp.wkv_scale is not None
     return dict(
         hash_ids=torch.from_numpy(inp.hash_ids).to(device),
         x=bits_to_device(inp.x, device),
         mask=None if inp.mask is None else torch.from_numpy(inp.mask).to(device),
-        wkv=bits_to_device(inp.wkv, device),
+        wkv=torch.from_numpy(inp.wkv).to(device) if fp8 else bits_to_device(inp.wkv, device),
         q=bits_to_device(inp.q, device),
         k=bits_to_device(inp.k, device),
+        wkv_scale=torch.from_numpy(inp.wkv_scale).to(device) if fp8 else None,
     )

@@ -77,6 +77,21 @@ typedef enum {
   ENGRAM_SCALE_E8M0 = 1      /* one E8M0 byte (2^(e-127)) per scale_block channels */
 } engram_scale_fmt;
 
+/* Format of the projection weight wkv.  The V4.1 tables and projections are
+ * FP8 (monishver11.github.io "DeepSeek's Other Modules", section "V4.1's two
+ * tables, reconciled"); the tables' format is MXFP8, E4M3 codes with one E8M0
+ * scale per 32 values (zhuai.tech "Engram in DeepSeek V4.1 Flash", section
+ * "Step 2").  ENGRAM_WKV_MXFP8 reads the weight in the same format along its
+ * input dimension:  W[j, k] = e4m3(wkv[j, k]) * 2^(wkv_scale[j, k/32] - 127).
+ * It requires an MXFP8 table (scale_fmt = ENGRAM_SCALE_E8M0, scale_block = 32):
+ * the projection then multiplies the table's codes and the weight's codes on
+ * the block-scaled FP8 tensor-core path, each with its own scales, with fp32
+ * accumulation; kv is rounded to bf16 as in the bf16 path. */
+typedef enum {
+  ENGRAM_WKV_BF16 = 0,       /* wkv: bf16 [N, K] */
+  ENGRAM_WKV_MXFP8 = 1       /* wkv: e4m3 codes [N, K]; wkv_scale: E8M0 [N, K/32] */
+} engram_wkv_fmt;
+
 typedef struct {
   int32_t dim;          /* per-stream hidden size (5120 in V4.1); multiple of 256, <= 5120 */
   int32_t hc_mult;      /* residual streams (4 in V4.1); 1..4 */
@@ -94,16 +109,21 @@ typedef struct {
                            (kv never reaches HBM) instead of a separate kernel.  Same bits
                            either way; on GB300 the separate kernel measured faster (the
                            epilogue work slows the power-capped MMA), so 0 is the default. */
+  int32_t wkv_fmt;      /* engram_wkv_fmt; ENGRAM_WKV_MXFP8 needs K a multiple of 128 and
+                           takes no fused epilogue (fuse_gate is ignored) */
 } engram_config;
 
 typedef struct {
   const uint8_t* table;     /* device, [R, head_dim] fp8-e4m3 codes */
   const void* scale;        /* device, [R, head_dim/scale_block] fp32 or uint8 E8M0 */
-  const uint16_t* wkv;      /* device, [dim*(hc_mult+1), n_cols*head_dim] bf16, the
-                               Linear's [out, in] weight: keys of stream s at rows
-                               s*dim .. s*dim+dim-1, the value at rows hc_mult*dim .. */
+  const void* wkv;          /* device, [dim*(hc_mult+1), n_cols*head_dim], the Linear's
+                               [out, in] weight: keys of stream s at rows s*dim ..
+                               s*dim+dim-1, the value at rows hc_mult*dim ..; bf16 bits
+                               (uint16_t), or e4m3 codes (uint8_t) for ENGRAM_WKV_MXFP8 */
   const uint16_t* q_weight; /* device, [hc_mult, dim] bf16 */
   const uint16_t* k_weight; /* device, [hc_mult, dim] bf16 */
+  const uint8_t* wkv_scale; /* device, [dim*(hc_mult+1), n_cols*head_dim/32] E8M0 for
+                               ENGRAM_WKV_MXFP8; ignored (may be NULL) for bf16 */
 } engram_weights;
 
 typedef struct engram_ctx engram_ctx;
@@ -111,12 +131,12 @@ typedef struct engram_ctx engram_ctx;
 /* Validates the configuration, allocates the context's scratch on the current
  * device (sized by max_tokens), forms the fp32 product q_weight*k_weight
  * (used only as a product, per the `Engram` excerpt) and copies wkv into a
- * buffer of its own (N*K*2 bytes) in 32 KB tiles of 256 rows x 64 columns,
- * each stored as the projection's shared-memory stage holds it, so that every
- * weight read of a forward call is one contiguous 32 KB stream.  The table and
- * scales are referenced, not copied, and must outlive the context; wkv,
- * q_weight and k_weight are read only here (a changed weight needs a new
- * context).  Synchronous.
+ * buffer of its own (N*K*2 bytes for bf16, N*K + N*K/32 for MXFP8) in 32 KB
+ * tiles of 256 rows x 128 bytes, each stored as the projection's shared-memory
+ * stage holds it, so that every weight read of a forward call is one
+ * contiguous 32 KB stream.  The table and scales are referenced, not copied,
+ * and must outlive the context; wkv, wkv_scale, q_weight and k_weight are read
+ * only here (a changed weight needs a new context).  Synchronous.
  * Returns ENGRAM_EINVAL / ENGRAM_EUNSUPPORTED for bad or unsupported shapes,
  * ENGRAM_ENOMEM if the scratch cannot be allocated, ENGRAM_ECUDA otherwise. */
 ENGRAM_API engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w);

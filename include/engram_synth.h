@@ -46,6 +46,15 @@ ENGRAM_SYNTH_API int32_t engram_synth_fill_table(uint8_t* table, float* scale, i
                                 uint64_t key_scales, const uint8_t* code_qtable,
                                 const float* scale_qtable, engram_synth_stream_t stream);
 
+/* E8M0 scales of rows [row_begin, row_end): `scale` (device, [R,
+ * head_dim/scale_block] uint8) takes e8m0_qtable[draw(key_scales, r*nb + b) >> 48],
+ * the same stream positions as the fp32 scales above.  e8m0_qtable: device,
+ * 65,536 uint8, built on the host.  Asynchronous on `stream`.  Returns 0, -1
+ * for a bad argument, -3 for a CUDA error. */
+ENGRAM_SYNTH_API int32_t engram_synth_fill_scales_e8m0(uint8_t* scale, int64_t row_begin, int64_t row_end,
+                                                       int32_t head_dim, int32_t scale_block, uint64_t key_scales,
+                                                       const uint8_t* e8m0_qtable, engram_synth_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

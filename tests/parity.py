@@ -25,16 +25,25 @@ def bf16_step(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, np.maximum(e - 8, -133))
 
 
-def kv_bound(e_bits, wkv_bits, kv_ref_bits, K: int, splits: int = 3):
+def weight_values(inp: synth.HostInputs) -> np.ndarray:
+    """The projection weight as float64 [N, K]: bf16 bits, or the MXFP8 codes
+    and scales (through the oracle's definition)."""
+    if inp.wkv_scale is None:
+        return O.bf16_value(inp.wkv)
+    return O.mxfp8_weight(inp.wkv, inp.wkv_scale)
+
+
+def kv_bound(e_bits, w_values, kv_ref_bits, K: int, splits: int = 3):
     """Per-element bound on |gpu kv - oracle kv|: one bf16 step at the oracle
     value plus the fp32 dot-product error bound gamma_n * sum_k |e_k W_jk|
     (Higham, "Accuracy and Stability of Numerical Algorithms", section 3.1),
-    with n = K/16 accumulator additions of 16-product MMA partials, 16 more for
-    the partial itself, and the split-K additions."""
-    n = K // 16 + 16 + splits
+    with n = K/16 accumulator additions of MMA partials (16 or 32 products
+    each), 32 more for the partial itself, and the split-K additions.
+    w_values: the weight as float64 [N, K] (weight_values)."""
+    n = K // 16 + 32 + splits
     u = 2.0 ** -24
     gamma = n * u / (1 - n * u)
-    absdot = np.abs(O.bf16_value(e_bits)) @ np.abs(O.bf16_value(wkv_bits)).T
+    absdot = np.abs(O.bf16_value(e_bits)) @ np.abs(np.asarray(w_values, dtype=np.float64)).T
     return bf16_step(O.bf16_value(kv_ref_bits)) + gamma * absdot
 
 
@@ -99,7 +108,7 @@ def check_layer(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, gpu_o
     gpu_gates = np.asarray(gpu_gates, dtype=np.float64).reshape(M, hc)
     gpu_kv = np.asarray(gpu_kv, dtype=np.uint16).reshape(M, -1)
     # 1. projection
-    bound = kv_bound(oracle_rows(w, inp, tok), inp.wkv, ref_kv, w.K)
+    bound = kv_bound(oracle_rows(w, inp, tok), weight_values(inp), ref_kv, w.K)
     kv_err = np.abs(O.bf16_value(gpu_kv) - O.bf16_value(ref_kv))
     far = kv_err > bound
     assert not far.any(), f"{what}: kv outside the bound at {np.argwhere(far)[:5].tolist()} ({far.sum()})"
@@ -140,10 +149,11 @@ def compact_rows(w: synth.Workload, ids: np.ndarray, seed: int | None = None):
     valid = (ids >= 0) & (ids < R)
     uniq = np.unique(ids[valid])
     if uniq.size:
-        codes, scales = synth.table_rows(seed, uniq, w.head_dim, w.scale_block)
+        codes, scales = synth.table_rows(seed, uniq, w.head_dim, w.scale_block, w.scale_fmt)
     else:
         codes = np.zeros((1, w.head_dim), np.uint8)
-        scales = np.ones((1, w.head_dim // w.scale_block), np.float32)
+        nb = w.head_dim // w.scale_block
+        scales = np.full((1, nb), 127, np.uint8) if w.scale_fmt == 1 else np.ones((1, nb), np.float32)
     out = np.full(ids.shape, -1, dtype=np.int64)
     out[valid] = np.searchsorted(uniq, ids[valid])
     return out, codes, scales
@@ -153,7 +163,7 @@ def oracle_rows(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray) -> np
     """Oracle gathered rows (bf16 bits [n, K]) of the tokens `tok`."""
     ids = inp.hash_ids.reshape(w.M, w.n_cols)[tok]
     cids, codes, scales = compact_rows(w, ids)
-    return O.lookup(cids, codes, scales, w.scale_block)
+    return O.lookup(cids, codes, scales, w.scale_block, w.scale_fmt)
 
 
 def oracle_tokens(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, eps: float | None = None):
@@ -165,7 +175,7 @@ def oracle_tokens(w: synth.Workload, inp: synth.HostInputs, tok: np.ndarray, eps
     x = inp.x.reshape(M, w.hc_mult, w.dim)[tok]
     mask = None if inp.mask is None else inp.mask.reshape(M)[tok]
     return O.forward(cids, x, codes, scales, inp.wkv, inp.q, inp.k, mask, scale_block=w.scale_block,
-                     eps=w.eps if eps is None else eps)
+                     scale_fmt=w.scale_fmt, eps=w.eps if eps is None else eps, wkv_scale=inp.wkv_scale)
 
 
 def sample_tokens(M: int, n: int, rng, must=()) -> np.ndarray:

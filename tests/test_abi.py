@@ -66,9 +66,10 @@ int main(void) {
   F(engram_config, dim); F(engram_config, hc_mult); F(engram_config, n_cols); F(engram_config, head_dim);
   F(engram_config, scale_block); F(engram_config, scale_fmt); F(engram_config, num_rows); F(engram_config, eps);
   F(engram_config, clamp); F(engram_config, max_tokens); F(engram_config, check_ids); F(engram_config, fuse_gate);
+  F(engram_config, wkv_fmt);
   printf("engram_weights %zu\n", sizeof(engram_weights));
   F(engram_weights, table); F(engram_weights, scale); F(engram_weights, wkv); F(engram_weights, q_weight);
-  F(engram_weights, k_weight);
+  F(engram_weights, k_weight); F(engram_weights, wkv_scale);
   printf("engram_hash_config %zu\n", sizeof(engram_hash_config));
   F(engram_hash_config, n_layers); F(engram_hash_config, max_ngram_size); F(engram_hash_config, n_heads);
   F(engram_hash_config, max_batch); F(engram_hash_config, max_len); F(engram_hash_config, vocab_size);
@@ -92,7 +93,7 @@ int main(void) {
 
 def test_host_only_entry_points(libs):
     lib = libs.engram()
-    assert lib.engram_abi_version() == 100
+    assert lib.engram_abi_version() == 101
     for code, text in ((0, b"ok"), (-1, b"invalid argument"), (-4, b"hash id outside the table"),
                        (-5, b"kernel wait timed out"), (-6, b"unsupported shape or format"), (7, b"unknown status")):
         assert lib.engram_status_string(code) == text

@@ -13,8 +13,28 @@ def test_splitmix64_known_answers():
 
 
 def test_workload_row_totals():
-    want = [100_776, 25_169_534, 402_659_764, 100_667_472, 384_016_682]
+    want = [100_776, 25_169_534, 402_659_764, 100_667_472, 384_016_682, 100_776, 25_169_534, 100_667_472]
     assert [w.num_rows() for w in synth.WORKLOADS] == want
+
+
+def test_mxfp8_inputs():
+    """The MXFP8 workloads: E8M0 table scales (the fp32 scales' stream
+    positions, rounded to powers of two), and an FP8 weight whose values have
+    about the bf16 weight's spread N(0, 1/K)."""
+    w = synth.workload("tiny_1x16_mxfp8")
+    assert (w.scale_block, w.scale_fmt, w.wkv_fmt) == (32, 1, 1)
+    rows = np.arange(0, 2000, 7)
+    _, s32 = synth.table_rows(w.seed, rows, w.head_dim, 32)
+    _, s8 = synth.table_rows(w.seed, rows, w.head_dim, 32, scale_fmt=1)
+    assert s8.dtype == np.uint8
+    assert np.all(np.abs(np.log2(s32.astype(np.float64)) - (s8.astype(np.float64) - 127)) <= 0.5 + 1e-9)
+    codes, scales = synth.make_wkv_mxfp8(w, rows_per_chunk=4096)
+    assert codes.shape == (w.N, w.K) and scales.shape == (w.N, w.K // 32)
+    assert set(np.unique(scales).tolist()) == {120, 121}
+    assert not np.any((codes & 0x7F) == 0x7F)                   # no NaN codes
+    from oracle import engram_oracle as O
+    W = O.mxfp8_weight(codes[:256], scales[:256])
+    assert abs(W.std() * np.sqrt(w.K) - 1.0) < 0.1
 
 
 def test_table_rows_deterministic_and_chunk_independent():
