@@ -216,6 +216,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// 16-byte shared-memory accesses by 32-bit shared address (the kernels compute
+// their shared-memory pointers by integer arithmetic, which hides the state
+// space from the compiler and would otherwise make these generic accesses).
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- block-scaled FP8
 // D[tmem] (+)= (A * sfA) * (B * sfB)^T with e4m3 A and B (K = 32 per
 // instruction) and one E8M0 scale per 32 K per row of A and of B, read from

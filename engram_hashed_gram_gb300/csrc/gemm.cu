@@ -18,8 +18,8 @@
 //  * no cluster, no multicast: the L2 serves the reuse of E and W across CTAs.
 // Variants: A_ROWS = 128 with 4 stages in general; for batches of at most 64
 // or 32 tokens the A box holds only 64 or 32 rows, and the shared memory that
-// frees goes to a deeper ring (5 or 6 stages), i.e. more of the weight stream
-// in flight per SM.  The MMA still reads 128 rows of A: rows past the box are
+// frees goes to a deeper ring (5 stages), i.e. more of the weight stream in
+// flight per SM.  The MMA still reads 128 rows of A: rows past the box are
 // whatever the neighbouring shared memory holds, their accumulator rows are
 // never stored, and a row of D depends on its own row of A only.  Rows of the
 // last M tile past M read as zeros (TMA bounds fill) and are not stored.
@@ -62,6 +62,12 @@ constexpr int kEpiGates = 32 * kEpiPitch;            // float [32][4]
 constexpr int kEpiFlags = kEpiGates + 32 * 16;       // int [32]
 constexpr int kEpiWarpBytes = kEpiFlags + 32 * 4;    // 3,200
 
+// Per epilogue warp, plain mode: a 32-row x 32-column fp32 tile (pitch 144
+// bytes, so that 16-byte writes of a row per lane and 16-byte reads of 8
+// lanes along a row are both free of bank conflicts).
+constexpr int kPlainPitch = 144;
+constexpr int kPlainWarpBytes = 32 * kPlainPitch;    // 4,608
+
 template <int A_ROWS, int STAGES, bool FP8 = false>
 struct Cfg {
   static constexpr int kABytes = A_ROWS * kBK * 2;                  // A_ROWS x 128 bytes either way
@@ -70,9 +76,9 @@ struct Cfg {
   static constexpr int kSfOffset = STAGES * (kABytes + kBBytes);
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
-  static constexpr int kEpiOffset = kBarOffset + 256;              // fused-mode staging, after the barriers
-  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kEpiOffset;
-  static constexpr size_t kSmemFused = kSmemBytes + 4 * kEpiWarpBytes;
+  static constexpr int kEpiOffset = kBarOffset + 256;              // epilogue staging, after the barriers
+  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kEpiOffset + 4 * kPlainWarpBytes;
+  static constexpr size_t kSmemFused = 1024 + kEpiOffset + 4 * kEpiWarpBytes;
   static constexpr bool kCanFuse = !FP8 && kSmemFused <= 232448;
   static_assert(!kCanFuse || kSmemFused <= 232448, "fused-mode shared memory");
   static_assert(!FP8 || STAGES * kSfColsPerStage + kSfCol0 <= kTmemCols, "scale columns");
@@ -152,33 +158,57 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned l
   atomicOr(err, kErrTimeout);
 }
 
-// kv (bf16) or the fp32 split-K partial sums of row m, columns [nt*256, nt*256 + 256).
-__device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m, int nt, int sp) {
+// kv (bf16) or the fp32 split-K partial sums of the warp's 32 rows (m0 ..
+// m0+31), columns [nt*256, nt*256 + 256).  tcgen05.ld gives each lane one
+// row; every 32-column chunk goes through the warp's shared-memory tile so
+// that the global stores are row segments: 8 lanes write one row's 128 bytes
+// of fp32 (4 rows per instruction), or 4 lanes its 64 bytes of bf16 (8 rows).
+__device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m0, int nt, int sp,
+                                               int lane, uint32_t stage) {
+  if (m0 >= a.M) return;                             // no row of this quarter is a token
+  const bool bf16 = a.out_mode == kOutBf16;
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
     tmem_ld_wait();
-    if (m < a.M) {
-      const int n0 = nt * kBN + c * 32;
-      if (a.out_mode == kOutBf16) {
-        uint4* dst = reinterpret_cast<uint4*>(a.kv + m * a.N + n0);
+    const uint32_t mine = stage + static_cast<uint32_t>(lane * kPlainPitch);
+    if (bf16) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          dst[j] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
-                              pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
-                              pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
-                              pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+      for (int j = 0; j < 4; ++j)
+        st_shared_v4(mine + 16 * j,
+                     make_uint4(pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                                pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                                pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                                pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]))));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_shared_v4(mine + 16 * j, make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
+    }
+    __syncwarp();
+    const int n0 = nt * kBN + c * 32;
+    if (bf16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = i * 8 + (lane >> 2);
+        const int q = lane & 3;
+        if (m0 + row < a.M) {
+          const uint4 v = ld_shared_v4(stage + static_cast<uint32_t>(row * kPlainPitch + q * 16));
+          *reinterpret_cast<uint4*>(a.kv + (m0 + row) * a.N + n0 + q * 8) = v;
         }
-      } else {
-        float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(sp) * a.M + m) * a.N + n0);
+      }
+    } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          dst[j] = make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
-                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      for (int i = 0; i < 8; ++i) {
+        const int row = i * 4 + (lane >> 3);
+        const int q = lane & 7;
+        if (m0 + row < a.M) {
+          const uint4 v = ld_shared_v4(stage + static_cast<uint32_t>(row * kPlainPitch + q * 16));
+          *reinterpret_cast<uint4*>(a.part + (static_cast<int64_t>(sp) * a.M + m0 + row) * a.N + n0 + q * 4) = v;
         }
       }
     }
+    __syncwarp();                                    // the tile is rewritten by the next chunk
   }
 }
 
@@ -586,7 +616,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ epilogue
     grid_dependency_wait();   // the outputs may still be read by an earlier kernel
     const int q = warp & 3;   // tensor-memory lane quarter this warp may read
-    uint8_t* epi = smem + C::kEpiOffset + (warp - 2) * kEpiWarpBytes;   // fused-mode staging of this warp
+    // this warp's staging tile
+    uint8_t* epi = smem + C::kEpiOffset + (warp - 2) * (FUSED ? kEpiWarpBytes : kPlainWarpBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -602,7 +633,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       if constexpr (!FUSED) {
-        plain_epilogue(a, t_row, m, nt, sp);
+        plain_epilogue(a, t_row, m - lane, nt, sp, lane, smem_u32(epi));
       } else if (nt < a.key_n_tiles) {
         fused_key_epilogue(a, t_row, m, nt * kBN, lane, reinterpret_cast<float*>(epi));
         fused_key_publish(a, m, mt, q, lane);
@@ -719,7 +750,7 @@ int gemm_a_rows(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : kBM); }
 
 bool gemm_can_fuse(int64_t M) {
   const int ar = gemm_a_rows(M);
-  return ar == 32 ? Cfg<32, 6>::kCanFuse : (ar == 64 ? Cfg<64, 5>::kCanFuse : Cfg<128, 4>::kCanFuse);
+  return ar == 32 ? Cfg<32, 5>::kCanFuse : (ar == 64 ? Cfg<64, 5>::kCanFuse : Cfg<128, 4>::kCanFuse);
 }
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
@@ -749,7 +780,7 @@ bool make_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t co
 cudaError_t gemm_prepare() {
   cudaError_t e = set_smem_attr<128, 4>();
   if (e == cudaSuccess) e = set_smem_attr<64, 5>();
-  if (e == cudaSuccess) e = set_smem_attr<32, 6>();
+  if (e == cudaSuccess) e = set_smem_attr<32, 5>();
   return e;
 }
 
@@ -781,7 +812,7 @@ cudaError_t launch_gemm(const void* rows, const CUtensorMap& tmB, const GemmArgs
             : make_tmap_bf16(&tmA, rows, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K),
                              static_cast<uint32_t>(ar));
   if (!mapped) return cudaErrorInvalidValue;
-  if (ar == 32) return launch_variant<32, 6>(tmA, tmB, a, ctas, stream);
+  if (ar == 32) return launch_variant<32, 5>(tmA, tmB, a, ctas, stream);
   if (ar == 64) return launch_variant<64, 5>(tmA, tmB, a, ctas, stream);
   return launch_variant<128, 4>(tmA, tmB, a, ctas, stream);
 }
