@@ -25,6 +25,7 @@ oracle alone as the reference arm.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -469,6 +470,141 @@ def run_hash(args, w):
                                                    "orders": [2, 3, 4], "heads": 8}}
 
 
+def _backbone(h, i, bw, w):
+    return (h.view(-1, w.dim) @ bw[i]).view(h.shape)
+
+
+def step_plain(layers, ids, x0, mask, bw, w):
+    """One step with each Engram layer's forward inline (for the equality check)."""
+    h = _backbone(x0, 0, bw, w)
+    h = layers[0].forward(ids[0], h, mask)
+    for i in range(1, 14):
+        h = _backbone(h, i, bw, w)
+    h = layers[1].forward(ids[1], h, mask)
+    return _backbone(h, 14, bw, w)
+
+
+def run_runahead(args, w):
+    """Times the run-ahead schedule (EngramRunAhead) against the same step with
+    each Engram layer's forward inline, around a backbone stand-in: two Engram
+    layers at the V4.1 positions (layers 1 and 14), one bf16 [4M, 5120] x
+    [5120, 5120] matmul (cuBLAS) for each of the 15 other layers up to layer
+    15.  The stand-in only occupies the GPU the way dense layers would; it is
+    not the model's backbone.  Both Engram layers share the workload's table
+    (their gathers touch different rows); each has its own weight.  Prints
+    one JSON line."""
+    import numpy as np
+    import torch
+    from engram_hashed_gram_gb300 import build as B
+    from engram_hashed_gram_gb300 import synth
+    from engram_hashed_gram_gb300 import synth_device as SD
+    from engram_hashed_gram_gb300.layer import EngramLayer, EngramRunAhead
+    B.build()
+    dev = torch.device("cuda", 0)
+    M = w.M
+    inp = synth.make_inputs(w)
+    table, scale = SD.make_table(w)
+    d = SD.upload_inputs(inp)
+    w2 = dataclasses.replace(w, seed=w.seed + 100)
+    wkv2 = SD.bits_to_device(synth.make_wkv(w2)) if w.wkv_fmt == 0 else None
+    kw = dict(max_tokens=M, eps=w.eps, scale_block=w.scale_block, scale_fmt=w.scale_fmt)
+    if w.wkv_fmt == 0:
+        layers = [EngramLayer(table, scale, d["wkv"], d["q"], d["k"], **kw),
+                  EngramLayer(table, scale, wkv2, d["q"], d["k"], **kw)]
+    else:
+        c2, s2 = synth.make_wkv_mxfp8(w2)
+        c2, s2 = torch.from_numpy(c2).to(dev), torch.from_numpy(s2).to(dev)
+        layers = [EngramLayer(table, scale, d["wkv"], d["q"], d["k"], wkv_scale=d["wkv_scale"], **kw),
+                  EngramLayer(table, scale, c2, d["q"], d["k"], wkv_scale=s2, **kw)]
+    rng = np.random.default_rng([w.seed, 31])
+    ids = [d["hash_ids"], torch.from_numpy(synth.make_hash_ids(w, rng=rng)).to(dev)]
+    x0, mask = d["x"], d["mask"]
+    g = torch.Generator(device=dev).manual_seed(5)
+    bw = [torch.randn((w.dim, w.dim), device=dev, dtype=torch.bfloat16, generator=g) * (w.dim ** -0.5)
+          for _ in range(15)]
+    same = torch.equal(step_plain(layers, ids, x0, mask, bw, w).view(torch.int16),
+                       step_plain(layers, ids, x0, mask, bw, w).view(torch.int16))
+    budgets = [0, 0] if args.sm_budget is None else [int(v) for v in str(args.sm_budget).split(",")]
+    if len(budgets) == 1:
+        budgets = budgets * 2
+    ra = EngramRunAhead(layers, max_tokens=M, sm_budget=budgets)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    backbone = lambda h, i: _backbone(h, i, bw, w)
+
+    def step_backbone():
+        h = x0
+        for i in range(15):
+            h = backbone(h, i)
+        return h
+
+    def set_budget(per_layer):
+        for lay, n in zip(layers, per_layer):
+            lay.set_sm_budget(n)
+
+    def step_serial():
+        set_budget([0, 0])                 # inline: the projections take every SM
+        h = backbone(x0, 0)
+        h = layers[0].forward(ids[0], h, mask)
+        for i in range(1, 14):
+            h = backbone(h, i)
+        h = layers[1].forward(ids[1], h, mask)
+        return backbone(h, 14)
+
+    def step_runahead():
+        set_budget(budgets)
+        ra.issue(ids)
+        h = backbone(x0, 0)
+        h = ra.apply(0, h, mask)
+        for i in range(1, 14):
+            h = backbone(h, i)
+        h = ra.apply(1, h, mask)
+        return backbone(h, 14)
+
+    def timed(fns):
+        """Median device ms of each step function, the three interleaved step
+        by step so that clock and power drift hit them alike."""
+        for _ in range(args.warmup):
+            for fn in fns:
+                fn()
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in fns]
+              for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for row in ev:
+            torch.cuda._sleep(int(2e6))         # the host queues the round ahead of the device
+            for fn, (a, b) in zip(fns, row):
+                flush.zero_()
+                a.record()
+                fn()
+                b.record()
+        torch.cuda.synchronize()
+        return [statistics.median(row[j][0].elapsed_time(row[j][1]) for row in ev) for j in range(len(fns))]
+
+    # the run-ahead result against the same step with each layer's forward inline
+    # under the same projection plan (the budget fixes the split-K plan)
+    ref = step_runahead()
+    set_budget(budgets)
+    same = same and torch.equal(step_plain(layers, ids, x0, mask, bw, w).view(torch.int16), ref.view(torch.int16))
+    t_bb, t_serial, t_ra = timed([step_backbone, step_serial, step_runahead])
+    set_budget(budgets)
+    ra_plan = [list(lay.plan(M)) for lay in layers]
+    for lay in layers:
+        st, _ = lay.sync_status()
+        if st != 0:
+            raise RuntimeError(f"status {st}")
+        lay.close()
+    engram = t_serial - t_bb
+    return {"component": "engram_runahead", "metric": "step ms with two Engram layers", "unit": "ms",
+            "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+            "backbone_only_ms": t_bb, "serial_ms": t_serial, "runahead_ms": t_ra,
+            "engram_inline_ms": engram, "engram_hidden_frac": (t_serial - t_ra) / engram if engram > 0 else None,
+            "bitwise_equal": bool(same), "dtype": "bf16" if w.wkv_fmt == 0 else "mxfp8",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "engram_layers": [1, 14],
+                       "engram_sm_budget": budgets, "engram_plan_runahead": ra_plan,
+                       "backbone_stand_in": f"15 x bf16 [{4 * M}, {w.dim}] x [{w.dim}, {w.dim}] matmul",
+                       "l2": "flushed between timed steps (256 MB write)"}}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,8 +614,13 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--component", choices=["layer", "hash"], default="layer",
-                    help="hash: time the n-gram hash (engram_hash) alone and print its own JSON line")
+    ap.add_argument("--component", choices=["layer", "hash", "runahead"], default="layer",
+                    help="hash: time the n-gram hash (engram_hash) alone; runahead: two Engram layers run "
+                         "ahead on a side stream vs inline, around a backbone stand-in; each prints its own "
+                         "JSON line")
+    ap.add_argument("--sm-budget", default=None,
+                    help="runahead: cap the Engram projections at this many SMs (engram_set_sm_budget): one "
+                         "count, or one per layer separated by commas (0 = all SMs)")
     ap.add_argument("--fuse-gate", action="store_true",
                     help="form the gate in the projection's epilogue (engram_config.fuse_gate)")
     ap.add_argument("--prime-base", type=int, default=None,
@@ -495,7 +636,6 @@ def main():
     from engram_hashed_gram_gb300 import synth
     w = synth.workload(int(args.workload) if args.workload.isdigit() else args.workload)
     if args.prime_base is not None:
-        import dataclasses
         w = dataclasses.replace(w, prime_base=args.prime_base, prime_skip=0)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -505,6 +645,10 @@ def main():
     if args.component == "hash":
         if rank == 0:
             print(json.dumps(run_hash(args, w)), flush=True)
+        return
+    if args.component == "runahead":
+        if rank == 0:
+            print(json.dumps(run_runahead(args, w)), flush=True)
         return
 
     if args.impl == "reference":

@@ -20,6 +20,7 @@ struct engram_ctx {
   engram_weights w;
   int device;
   int num_sms;
+  int sm_budget;              // SMs the projection's persistent grid may occupy (engram_set_sm_budget)
   int32_t K;
   int32_t N;
   float* wprod;               // [hc, dim] fp32
@@ -62,7 +63,8 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
   p.n_tiles = c->N / kBN;
   const int32_t kbt = c->K / (c->fp8 ? 128 : kBK);
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  auto waves = [&](int64_t units) { return (units + c->num_sms - 1) / c->num_sms; };
+  const int64_t sms = c->sm_budget;
+  auto waves = [&](int64_t units) { return (units + sms - 1) / sms; };
   int32_t best = 1;
   int64_t best_cost = waves(tiles) * kbt;
   if (M <= kSplitMaxTokens && M <= c->part_tokens) {
@@ -86,7 +88,7 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
     best = forced;
   p.splits = best;
   p.units = tiles * best;
-  p.ctas = static_cast<int32_t>(p.units < c->num_sms ? p.units : c->num_sms);
+  p.ctas = static_cast<int32_t>(p.units < sms ? p.units : sms);
   return p;
 }
 
@@ -301,6 +303,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
     delete ctx;
     return ENGRAM_EUNSUPPORTED;
   }
+  ctx->sm_budget = ctx->num_sms;
   const int64_t mt = c.max_tokens > 0 ? c.max_tokens : 1;
   ctx->part_tokens = mt < kSplitMaxTokens ? mt : kSplitMaxTokens;
   const size_t hcd = static_cast<size_t>(c.hc_mult) * c.dim;
@@ -461,6 +464,12 @@ engram_status engram_stage_times(engram_ctx* ctx, float* ms) {
   if (cudaEventSynchronize(ctx->ev[3]) != cudaSuccess) return ENGRAM_ECUDA;
   for (int i = 0; i < 3; ++i)
     if (cudaEventElapsedTime(&ms[i], ctx->ev[i], ctx->ev[i + 1]) != cudaSuccess) return ENGRAM_ECUDA;
+  return ENGRAM_OK;
+}
+
+engram_status engram_set_sm_budget(engram_ctx* ctx, int32_t sms) {
+  if (ctx == nullptr || sms < 0) return ENGRAM_EINVAL;
+  ctx->sm_budget = (sms == 0 || sms > ctx->num_sms) ? ctx->num_sms : sms;
   return ENGRAM_OK;
 }
 

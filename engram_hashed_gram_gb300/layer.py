@@ -161,6 +161,10 @@ class EngramLayer:
         check(self._lib.engram_plan(self._ctx, m_tokens, ctypes.byref(s), ctypes.byref(c)), "engram_plan")
         return s.value, c.value
 
+    def set_sm_budget(self, sms: int):
+        """At most `sms` SMs for the projection's grid (0 = all of them)."""
+        check(self._lib.engram_set_sm_budget(self._ctx, sms), "engram_set_sm_budget")
+
     def enable_stage_timing(self, enable=True):
         check(self._lib.engram_enable_stage_timing(self._ctx, 1 if enable else 0), "engram_enable_stage_timing")
 
@@ -225,3 +229,75 @@ class EngramHasher:
                                     _ptr(input_ids), _ptr(token_mask), start_pos, _ptr(out), B, L, _stream(stream)),
               "engram_hash")
         return out
+
+
+class EngramRunAhead:
+    """Run-ahead schedule of the Engram layers of one model step.
+
+    The lookup and the projection depend only on the token ids, so they can
+    run ahead of the backbone; only the gate needs the hidden state at the
+    layer's entry (zhuai.tech "Engram in DeepSeek V4.1 Flash", section "Run
+    projection early: overlap CPU work with the GPU"; monishver11.github.io
+    "DeepSeek's Other Modules", section "Serving cost: gathers, not FLOPs": the
+    addresses are known early, so the fetch overlaps the first block).
+
+    issue(hash_ids_per_layer) queues every layer's engram_lookup_project on a
+    side stream as soon as the ids are ready on the caller's stream;
+    apply(i, x, ...) makes the caller's stream wait for layer i's kv and runs
+    engram_gate_apply there.  The result equals each layer's engram_forward
+    bit for bit.  One kv buffer per layer ([max_tokens, N] bf16) is owned
+    here; the next issue() waits for the caller's stream, so it never
+    overwrites a kv an earlier apply() still reads."""
+
+    def __init__(self, layers, max_tokens: int, sm_budget=None):
+        """sm_budget: if given (one count for every layer, or one per layer),
+        the layers' projections are capped at that many SMs
+        (engram_set_sm_budget; 0 = all), leaving the rest to the caller's
+        stream.  A layer far from the step's start can trickle on a few SMs
+        while the backbone runs; the first one is needed soon and takes all."""
+        if not layers:
+            raise ValueError("at least one layer")
+        self.layers = list(layers)
+        self.device = self.layers[0].device
+        for lay in self.layers:
+            if lay.device != self.device:
+                raise ValueError("all layers must be on one device")
+        self.max_tokens = max_tokens
+        self.side = torch.cuda.Stream(self.device)
+        self._kv = [torch.empty((max_tokens, lay.N), dtype=torch.bfloat16, device=self.device) for lay in self.layers]
+        self._ready = [torch.cuda.Event() for _ in self.layers]
+        self._shape = None
+        if sm_budget is not None:
+            budgets = list(sm_budget) if isinstance(sm_budget, (list, tuple)) else [sm_budget] * len(self.layers)
+            if len(budgets) != len(self.layers):
+                raise ValueError("one SM budget per layer")
+            for lay, b in zip(self.layers, budgets):
+                lay.set_sm_budget(int(b))
+
+    def issue(self, hash_ids_per_layer, stream=None):
+        """Queues lookup_project of every layer on the side stream, after the
+        work already queued on `stream` (the current stream by default)."""
+        if len(hash_ids_per_layer) != len(self.layers):
+            raise ValueError("one hash-id tensor per layer")
+        main = torch.cuda.current_stream(self.device) if stream is None else stream
+        B, T = hash_ids_per_layer[0].shape[0], hash_ids_per_layer[0].shape[1]
+        if B * T > self.max_tokens:
+            raise ValueError(f"{B * T} tokens exceed max_tokens {self.max_tokens}")
+        self.side.wait_stream(main)
+        for i, (lay, ids) in enumerate(zip(self.layers, hash_ids_per_layer)):
+            if ids.shape[0] != B or ids.shape[1] != T:
+                raise ValueError("every layer's hash ids must cover the same [B, T]")
+            kv = self._kv[i][: B * T].view(B, T, lay.N)
+            lay.lookup_project(ids, kv=kv, stream=self.side)
+            self._ready[i].record(self.side)
+        self._shape = (B, T)
+
+    def apply(self, i, x, token_mask=None, out=None, gates=None, stream=None):
+        """Layer i at its entry: waits (on `stream`) for its kv, then gates."""
+        if self._shape is None:
+            raise RuntimeError("issue() first")
+        B, T = self._shape
+        main = torch.cuda.current_stream(self.device) if stream is None else stream
+        main.wait_event(self._ready[i])
+        kv = self._kv[i][: B * T].view(B, T, self.layers[i].N)
+        return self.layers[i].gate_apply(kv, x, token_mask, out=out, gates=gates, stream=main)

@@ -182,6 +182,14 @@ ENGRAM_API engram_status engram_sync_status(engram_ctx* ctx, engram_stream_t str
  * this context's device (for tests and benchmarks; queues nothing). */
 ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, int32_t* splits, int32_t* ctas);
 
+/* Caps the number of SMs the projection's persistent grid occupies (and that
+ * its split-K plan is made for) at `sms`; 0 or more than the device has
+ * restores all of them.  For running lookup_project ahead on a side stream
+ * while other kernels use the rest of the GPU.  The plan, and with it the
+ * summation order of kv, may change with the budget.  Host-only; affects
+ * later calls.  ENGRAM_EINVAL for a NULL context or a negative count. */
+ENGRAM_API engram_status engram_set_sm_budget(engram_ctx* ctx, int32_t sms);
+
 /* Stage timing, for benchmarks.  With enable != 0 the context creates CUDA
  * events and every later engram_forward / engram_lookup_project records one
  * before the gather and one after each of its kernels on the call's stream;
