@@ -21,6 +21,8 @@
 // them up locally.  The result does not depend on timing, and the
 // split-K path rounds kv to bf16 exactly as the separate reduction kernel does,
 // so engram_forward and lookup_project + gate_apply agree bit for bit.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "internal.cuh"
 
@@ -185,6 +187,131 @@ __global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const Ga
   }
 }
 
+// The same layer step for large batches: one CTA per token and no cluster.
+// Warp w owns blocks w*BPW .. w*BPW+BPW-1 of every stream (lane l channels
+// 8l..8l+7 of each), so the per-block sums, the butterflies and the block
+// order are exactly those of gate_residual_kernel and the two give the same
+// bits.  Every load of the token (x, key and value, 16 bytes each) is issued
+// before any arithmetic, so a CTA keeps (2 HC + 1) * BPW * 16 bytes per thread
+// in flight; with two CTAs per SM that covers HBM latency.  kv only (no
+// split-K partials: large batches do not split K).
+template <int BPW>
+__global__ void __launch_bounds__(kMaxBlocks / BPW * 32, 2) gate_residual_wide_kernel(const GateArgs a) {
+  __shared__ float red[kMaxBlocks][3 * kMaxHc];
+  __shared__ float tot[3 * kMaxHc];
+  __shared__ float gate_s[kMaxHc];
+
+  const int64_t m = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int D = a.dim;
+  const int HC = a.hc;
+  const int nblocks = D / kBlockCh;
+  const int64_t N = static_cast<int64_t>(D) * (HC + 1);
+  const uint16_t* xm = a.x + m * HC * D;
+  uint16_t* om = a.out + m * HC * D;
+  int d0[BPW];
+#pragma unroll
+  for (int j = 0; j < BPW; ++j) d0[j] = (warp * BPW + j) * kBlockCh + lane * 8;
+
+  if (a.mask != nullptr && a.mask[m] == 0) {
+    grid_dependency_wait();
+    if (om != xm) {
+#pragma unroll
+      for (int j = 0; j < BPW; ++j)
+        for (int s = 0; s < HC; ++s)
+          *reinterpret_cast<uint4*>(om + s * D + d0[j]) = __ldg(reinterpret_cast<const uint4*>(xm + s * D + d0[j]));
+    }
+    if (a.gates != nullptr && threadIdx.x < HC) a.gates[m * HC + threadIdx.x] = 0.0f;
+    grid_launch_dependents();
+    return;
+  }
+
+  uint4 xr[BPW][kMaxHc], kr[BPW][kMaxHc], vr[BPW];
+#pragma unroll
+  for (int j = 0; j < BPW; ++j)
+#pragma unroll
+    for (int s = 0; s < kMaxHc; ++s)
+      if (s < HC) xr[j][s] = __ldg(reinterpret_cast<const uint4*>(xm + s * D + d0[j]));
+  grid_dependency_wait();        // kv comes from the projection
+  grid_launch_dependents();
+  const uint16_t* kvm = a.kv + m * N;
+#pragma unroll
+  for (int j = 0; j < BPW; ++j) {
+#pragma unroll
+    for (int s = 0; s < kMaxHc; ++s)
+      if (s < HC) kr[j][s] = __ldg(reinterpret_cast<const uint4*>(kvm + s * D + d0[j]));
+    vr[j] = __ldg(reinterpret_cast<const uint4*>(kvm + static_cast<int64_t>(HC) * D + d0[j]));
+  }
+
+#pragma unroll
+  for (int j = 0; j < BPW; ++j) {
+    float sums[3 * kMaxHc];
+#pragma unroll
+    for (int s = 0; s < kMaxHc; ++s) {
+      sums[3 * s] = sums[3 * s + 1] = sums[3 * s + 2] = 0.0f;
+      if (s < HC) {
+        float h[8], k[8];
+        unpack8(xr[j][s], h);
+        unpack8(kr[j][s], k);
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0[j]));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0[j]) + 1);
+        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          sh = fmaf(h[c], h[c], sh);
+          sk = fmaf(k[c], k[c], sk);
+          sd = fmaf(__fmul_rn(h[c], w[c]), k[c], sd);
+        }
+        sums[3 * s] = sh;
+        sums[3 * s + 1] = sk;
+        sums[3 * s + 2] = sd;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 3 * kMaxHc; ++i) {
+      float v = sums[i];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      if (lane == 0) red[warp * BPW + j][i] = v;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 3 * HC) {            // one (stream, quantity) per thread, blocks in order
+    float acc = 0.0f;
+    for (int b = 0; b < nblocks; ++b) acc += red[b][threadIdx.x];
+    tot[threadIdx.x] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < HC) {
+    const int t = threadIdx.x;
+    const float g = engram_gate(tot[3 * t], tot[3 * t + 1], tot[3 * t + 2], D, a.eps, a.clamp, a.inv_sqrt_dim);
+    gate_s[t] = g;
+    if (a.gates != nullptr) a.gates[m * HC + t] = g;
+  }
+  __syncthreads();
+
+#pragma unroll
+  for (int j = 0; j < BPW; ++j) {
+    float v[8];
+    unpack8(vr[j], v);
+#pragma unroll
+    for (int s = 0; s < kMaxHc; ++s) {
+      if (s < HC) {
+        const float g = gate_s[s];
+        float h[8];
+        unpack8(xr[j][s], h);
+        uint4 o;
+        o.x = pack_bf16x2(fmaf(g, v[0], h[0]), fmaf(g, v[1], h[1]));
+        o.y = pack_bf16x2(fmaf(g, v[2], h[2]), fmaf(g, v[3], h[3]));
+        o.z = pack_bf16x2(fmaf(g, v[4], h[4]), fmaf(g, v[5], h[5]));
+        o.w = pack_bf16x2(fmaf(g, v[6], h[6]), fmaf(g, v[7], h[7]));
+        *reinterpret_cast<uint4*>(om + s * D + d0[j]) = o;
+      }
+    }
+  }
+}
+
 __global__ void reduce_partials_kernel(const float* __restrict__ part, int splits, int64_t MN,
                                        uint16_t* __restrict__ kv) {
   grid_dependency_wait();
@@ -218,9 +345,31 @@ int gate_cluster_size(int dim) {
   return nblocks % 4 == 0 ? 4 : (nblocks % 2 == 0 ? 2 : 1);
 }
 
+// Batches of at least this many tokens (with bf16 kv) take the one-CTA-per-
+// token kernel; smaller ones spread each token over a cluster for latency
+// (measured on GB300: 512 tokens 25.3 -> 20.5 us, 4096 tokens 167 -> 98 us,
+// 16384 tokens 688 -> 378 us).  ENGRAM_GATE_WIDE_MIN overrides it for
+// measurements.
+int64_t gate_wide_min_tokens() {
+  static const int64_t v = [] {
+    const char* e = std::getenv("ENGRAM_GATE_WIDE_MIN");
+    return e != nullptr ? static_cast<int64_t>(std::atoll(e)) : int64_t{256};
+  }();
+  return v;
+}
+
 cudaError_t launch_gate(const GateArgs& a_in, cudaStream_t stream) {
   if (a_in.M == 0) return cudaSuccess;
   GateArgs a = a_in;
+  const int nblocks = a.dim / kBlockCh;
+  if (a.part == nullptr && a.M >= gate_wide_min_tokens()) {
+    a.cluster = 1;
+    const dim3 grid(static_cast<unsigned>(a.M));
+    if (nblocks % 2 == 0)
+      return launch_pdl(gate_residual_wide_kernel<2>, grid, dim3(static_cast<unsigned>(nblocks / 2 * 32)), 0, stream,
+                        1, a);
+    return launch_pdl(gate_residual_wide_kernel<1>, grid, dim3(static_cast<unsigned>(nblocks * 32)), 0, stream, 1, a);
+  }
   a.cluster = gate_cluster_size(a.dim);
   const unsigned threads = static_cast<unsigned>(a.dim / kBlockCh / a.cluster * 32);
   const dim3 grid(static_cast<unsigned>(a.M * a.cluster));
