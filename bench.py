@@ -314,38 +314,70 @@ def run_ours(args, w, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"engram_forward reported status {st}")
 
-    # ---- end to end: pinned host inputs, copies inside the timed region
-    h_ids = inp_pinned(torch, inp.hash_ids)
-    h_x = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
-    h_mask = None if inp.mask is None else torch.from_numpy(inp.mask).pin_memory()
-    h_out = torch.empty(h_x.shape, dtype=torch.int16).pin_memory()
-    d_ids = torch.empty_like(ids)
-    d_x = torch.empty(x.shape, dtype=torch.int16, device=dev)
-    d_mask = None if mask is None else torch.empty_like(mask)
-    d_out = torch.empty_like(d_x)
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # ---- end to end, through the public call with host buffers: every step
+    # copies its inputs (x, ids and mask, packed in one pinned buffer) to the
+    # device and its output back.  Two device buffer sets and two copy streams
+    # let step i+1's upload and step i-1's download overlap step i's compute,
+    # as a serving loop would.  No L2 flush here: each step streams the whole
+    # weight (larger than L2) and its inputs arrive from the host.
+    nb_x, nb_ids = inp.x.nbytes, inp.hash_ids.nbytes
+    nb_m = 0 if inp.mask is None else inp.mask.nbytes
+    nb_in = (nb_x + nb_ids + nb_m + 15) // 16 * 16
+    h_in = torch.zeros(nb_in, dtype=torch.uint8).pin_memory()
+    h_in[:nb_x].copy_(torch.from_numpy(inp.x.reshape(-1).view(np.uint8)))
+    h_in[nb_x:nb_x + nb_ids].copy_(torch.from_numpy(inp.hash_ids.reshape(-1).view(np.uint8)))
+    if nb_m:
+        h_in[nb_x + nb_ids:nb_x + nb_ids + nb_m].copy_(torch.from_numpy(inp.mask.reshape(-1)))
+    d_in = [torch.empty(nb_in, dtype=torch.uint8, device=dev) for _ in range(2)]
+    views = []
+    for buf in d_in:
+        vx = buf[:nb_x].view(torch.bfloat16).view(x.shape)
+        vi = buf[nb_x:nb_x + nb_ids].view(torch.int64).view(ids.shape)
+        vm = buf[nb_x + nb_ids:nb_x + nb_ids + nb_m].view(mask.shape) if nb_m else None
+        views.append((vi, vx, vm))
+    d_out = [torch.empty_like(x) for _ in range(2)]
+    h_out = [torch.empty(x.shape, dtype=torch.int16).pin_memory() for _ in range(2)]
+    up_s, down_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        d_ids.copy_(h_ids, non_blocking=True)
-        d_x.copy_(h_x, non_blocking=True)
-        if d_mask is not None:
-            d_mask.copy_(h_mask, non_blocking=True)
-        layer.forward(d_ids, d_x, d_mask, out=d_out)
-        h_out.copy_(d_out, non_blocking=True)
+    def e2e_run(n):
+        """n pipelined steps; returns the device milliseconds from the first
+        upload to the last download.  Uploads and downloads run on their own
+        streams (the two copy directions overlap each other and the steps)."""
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        uploaded = [torch.cuda.Event() for _ in range(n)]
+        computed = [torch.cuda.Event() for _ in range(n)]
+        downloaded = [torch.cuda.Event() for _ in range(n)]
+        up_s.wait_stream(stream)
+        down_s.wait_stream(stream)
+        t0.record(up_s)
+        down_s.wait_event(t0)
+        for i in range(n):
+            b = i % 2
+            if i >= 2:
+                up_s.wait_event(computed[i - 2])           # step i-2 has read input buffer b
+            with torch.cuda.stream(up_s):
+                d_in[b].copy_(h_in, non_blocking=True)
+                uploaded[i].record(up_s)
+            stream.wait_event(uploaded[i])
+            if i >= 2:
+                stream.wait_event(downloaded[i - 2])       # output buffer b is back on the host
+            vi, vx, vm = views[b]
+            layer.forward(vi, vx, vm, out=d_out[b])
+            computed[i].record(stream)
+            down_s.wait_event(computed[i])
+            with torch.cuda.stream(down_s):
+                h_out[b].copy_(d_out[b].view(torch.int16), non_blocking=True)
+                downloaded[i].record(down_s)
+        t1.record(down_s)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        e2e_ev[i][0].record(stream)
-        e2e_step()
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-    if not np.array_equal(h_out.numpy().view(np.uint16), out.view(torch.int16).cpu().numpy().view(np.uint16)):
+    e2e_run(max(3, args.warmup))
+    e2e_ms = e2e_run(args.steps)
+    last = (args.steps - 1) % 2
+    if not np.array_equal(h_out[last].numpy().view(np.uint16), out.view(torch.int16).cpu().numpy().view(np.uint16)):
         raise RuntimeError("end-to-end output differs from the device-resident run")
-    h2d = inp.hash_ids.nbytes + inp.x.nbytes + (0 if inp.mask is None else inp.mask.nbytes)
+    h2d = nb_in
     d2h = inp.x.nbytes
 
     # ---- aggregate over ranks
@@ -389,7 +421,9 @@ def run_ours(args, w, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.wkv_fmt == 0 else "mxfp8", "data": "synthetic",
         "config": config_of(w),
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "schedule": "each step uploads its inputs and downloads its output; upload and download streams "
+                            "overlap the next upload and the previous download with the step (two buffer sets)"},
         "gpu_launches": 3 * args.steps,
         "roofline": roof,
         "layer_roofline": {"bytes": lbytes, "flops": lflops, "roofline_us": 1e6 * t_roof,
