@@ -28,6 +28,7 @@ SCALE_F32 = 0
 SCALE_E8M0 = 1
 WKV_BF16 = 0
 WKV_MXFP8 = 1
+TEST_HOLD_GATE_FLAGS = 1
 
 
 class EngramConfig(ctypes.Structure):
@@ -84,6 +85,7 @@ ENGRAM_FUNCS = {
     "engram_sync_status": (c_int32, [c_void_p, c_void_p, POINTER(c_int64)]),
     "engram_plan": (c_int32, [c_void_p, c_int64, POINTER(c_int32), POINTER(c_int32)]),
     "engram_set_sm_budget": (c_int32, [c_void_p, c_int32]),
+    "engram_test_hook": (c_int32, [c_void_p, c_int32]),
     "engram_forward_noalloc": (c_int32, [POINTER(EngramConfig), POINTER(EngramWeights), c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_int64, c_int64, c_void_p]),
     "engram_hash": (c_int32, [POINTER(EngramHashConfig), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,

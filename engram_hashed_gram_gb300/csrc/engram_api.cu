@@ -21,6 +21,7 @@ struct engram_ctx {
   int device;
   int num_sms;
   int sm_budget;              // SMs the projection's persistent grid may occupy (engram_set_sm_budget)
+  int32_t test_hooks;         // engram_test_hook bits
   int32_t K;
   int32_t N;
   float* wprod;               // [hc, dim] fp32
@@ -189,6 +190,7 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
     a.counters = c->counters;
     a.gates = c->gates;
     a.key_n_tiles = c->cfg.hc_mult * c->cfg.dim / kBN;
+    a.hold_ready_flags = (c->test_hooks & ENGRAM_TEST_HOLD_GATE_FLAGS) != 0 ? 1 : 0;
     a.dim = c->cfg.dim;
     a.hc = c->cfg.hc_mult;
     a.eps = c->cfg.eps;
@@ -464,6 +466,12 @@ engram_status engram_stage_times(engram_ctx* ctx, float* ms) {
   if (cudaEventSynchronize(ctx->ev[3]) != cudaSuccess) return ENGRAM_ECUDA;
   for (int i = 0; i < 3; ++i)
     if (cudaEventElapsedTime(&ms[i], ctx->ev[i], ctx->ev[i + 1]) != cudaSuccess) return ENGRAM_ECUDA;
+  return ENGRAM_OK;
+}
+
+engram_status engram_test_hook(engram_ctx* ctx, int32_t hooks) {
+  if (ctx == nullptr || (hooks & ~ENGRAM_TEST_HOLD_GATE_FLAGS) != 0) return ENGRAM_EINVAL;
+  ctx->test_hooks = hooks;
   return ENGRAM_OK;
 }
 

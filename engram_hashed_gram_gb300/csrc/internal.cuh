@@ -101,6 +101,7 @@ struct GemmArgs {
   float* gates;          // [M, 4] the gates of every row, formed by the last key warp of its quarter
   uint32_t* counters;    // [m_tiles, 8]: key tiles done per lane quarter, then gates-ready flags; zeroed by the gather
   int32_t key_n_tiles;   // n-tiles of the keys (hc*dim/256); every key unit precedes every value unit
+  int32_t hold_ready_flags;  // test hook (engram_test_hook): never raise the gates-ready flags
   int32_t dim;
   int32_t hc;
   float eps;

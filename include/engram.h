@@ -190,6 +190,16 @@ ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, in
  * later calls.  ENGRAM_EINVAL for a NULL context or a negative count. */
 ENGRAM_API engram_status engram_set_sm_budget(engram_ctx* ctx, int32_t sms);
 
+/* Failure-detection test hook.  ENGRAM_TEST_HOLD_GATE_FLAGS makes the fused
+ * gate epilogue (fuse_gate with a single-pass plan) never raise its
+ * gates-ready flags, so that the value tiles' bounded wait runs out: the
+ * call's output is then invalid, engram_sync_status() returns
+ * ENGRAM_ETIMEOUT, and the context stays usable once the hook is cleared.
+ * Nothing faults, traps or hangs; the wait ends after two seconds.  0 clears
+ * the hooks.  ENGRAM_EINVAL for a NULL context or unknown bits. */
+#define ENGRAM_TEST_HOLD_GATE_FLAGS 1
+ENGRAM_API engram_status engram_test_hook(engram_ctx* ctx, int32_t hooks);
+
 /* Stage timing, for benchmarks.  With enable != 0 the context creates CUDA
  * events and every later engram_forward / engram_lookup_project records one
  * before the gather and one after each of its kernels on the call's stream;

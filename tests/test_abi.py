@@ -111,6 +111,7 @@ def test_host_only_entry_points(libs):
     assert lib.engram_sync_status(None, None, None) == -1
     assert lib.engram_plan(None, 1, None, None) == -1
     assert lib.engram_set_sm_budget(None, 8) == -1
+    assert lib.engram_test_hook(None, 1) == -1
     assert lib.engram_enable_stage_timing(None, 1) == -1
     assert lib.engram_stage_times(None, None) == -1
     assert lib.engram_hash(None, None, None, None, None, None, None, None, 0, None, 1, 1, None) == -1

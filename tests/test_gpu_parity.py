@@ -242,3 +242,35 @@ def test_wide_gate_kernel_matches_cluster_kernel(tiny):
     summary = P.check_layer(w, inp, np.arange(1024), SD.device_bits(out_wide), g_wide.cpu().numpy(),
                             SD.device_bits(kv), "wide gate 1024 tokens")
     print(summary)
+
+
+def test_bounded_wait_runs_out_and_the_context_recovers(tiny):
+    """Failure detection without a fault: with the test hook, the fused
+    epilogue never raises its gates-ready flags, the value tiles' bounded wait
+    (two seconds) runs out, every role of the projection leaves its loop, and
+    engram_sync_status() reports ENGRAM_ETIMEOUT.  The next call on the same
+    context is correct again."""
+    import time
+    from engram_hashed_gram_gb300 import _lib
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    w, inp = _inputs(tiny, 1, 200, seed=6)
+    ids, x, _ = _dev(inp)
+    dev = tiny["dev"]
+    fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=256, fuse_gate=True)
+    try:
+        assert fused.plan(200)[0] == 1                       # single pass: the fused epilogue runs
+        assert _lib.engram().engram_test_hook(fused._ctx, _lib.TEST_HOLD_GATE_FLAGS) == 0
+        t0 = time.perf_counter()
+        fused.forward(ids, x)
+        st, _ = fused.sync_status()
+        elapsed = time.perf_counter() - t0
+        assert st == _lib.ENGRAM_ETIMEOUT, st
+        assert elapsed < 20.0
+        assert _lib.engram().engram_test_hook(fused._ctx, 0) == 0
+        out = fused.forward(ids, x)
+        st, _ = fused.sync_status()
+        assert st == 0
+        ref = tiny["layer"].forward(ids, x)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    finally:
+        fused.close()
