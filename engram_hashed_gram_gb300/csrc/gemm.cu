@@ -104,8 +104,19 @@ __device__ __forceinline__ void raster(const GemmArgs& a, int64_t t, int n_count
 // before every value tile: a value tile waits only for units with smaller
 // indices, and by the time any CTA reaches the value tiles nearly all key
 // tiles are done.
+__device__ __forceinline__ bool remainder_unit(const GemmArgs& a, int64_t u) {
+  return a.rem_splits > 0 && u >= a.full_units;
+}
+
 template <bool FUSED>
 __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& mt, int& nt, int& sp) {
+  if (!FUSED && remainder_unit(a, u)) {             // a remainder unit: sp is its K range
+    const int64_t j = u - a.full_units;
+    sp = static_cast<int>(j % a.rem_splits);
+    const int64_t tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
+    raster(a, tiles - a.rem_tiles + j / a.rem_splits, a.n_tiles, mt, nt);
+    return;
+  }
   sp = static_cast<int>(u % a.splits);
   const int64_t t = u / a.splits;
   if constexpr (FUSED) {
@@ -119,6 +130,17 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& m
     return;
   }
   raster(a, t, a.n_tiles, mt, nt);
+}
+
+// K blocks of unit u: [first, first + count).
+__device__ __forceinline__ void unit_kb(const GemmArgs& a, int64_t u, int sp, int& first, int& count) {
+  if (remainder_unit(a, u)) {
+    first = sp * a.rem_kb;
+    count = a.rem_kb;
+  } else {
+    first = sp * a.kb_per_split;
+    count = a.kb_per_split;
+  }
 }
 
 // The weight tile (N tile nt, K block kb) into a B stage: one contiguous 32 KB
@@ -163,10 +185,13 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned l
 // row; every 32-column chunk goes through the warp's shared-memory tile so
 // that the global stores are row segments: 8 lanes write one row's 128 bytes
 // of fp32 (4 rows per instruction), or 4 lanes its 64 bytes of bf16 (8 rows).
+// tile / tile_stride: instead of the output, the fp32 sums go to this 32-row
+// block (row r at tile + r * tile_stride), as for a remainder unit.
 __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m0, int nt, int sp,
-                                               int lane, uint32_t stage) {
+                                               int lane, uint32_t stage, float* tile = nullptr,
+                                               int64_t tile_stride = 0) {
   if (m0 >= a.M) return;                             // no row of this quarter is a token
-  const bool bf16 = a.out_mode == kOutBf16;
+  const bool bf16 = tile == nullptr && a.out_mode == kOutBf16;
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
@@ -204,7 +229,9 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
         const int q = lane & 7;
         if (m0 + row < a.M) {
           const uint4 v = ld_shared_v4(stage + static_cast<uint32_t>(row * kPlainPitch + q * 16));
-          *reinterpret_cast<uint4*>(a.part + (static_cast<int64_t>(sp) * a.M + m0 + row) * a.N + n0 + q * 4) = v;
+          float* dst = tile != nullptr ? tile + row * tile_stride + c * 32 + q * 4
+                                       : a.part + (static_cast<int64_t>(sp) * a.M + m0 + row) * a.N + n0 + q * 4;
+          *reinterpret_cast<uint4*>(dst) = v;
         }
       }
     }
@@ -502,13 +529,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // the gathered rows are still being written.
       int pre = 0;
       if (static_cast<int64_t>(blockIdx.x) < a.units) {
-        int mt, nt, sp;
+        int mt, nt, sp, kf, kn;
         unit_coords<FUSED>(a, blockIdx.x, mt, nt, sp);
-        pre = min(kStages, a.kb_per_split);
+        unit_kb(a, blockIdx.x, sp, kf, kn);
+        pre = min(kStages, kn);
         for (int i = 0; i < pre; ++i) {   // fresh ring: every stage is free
           mbar_arrive_expect_tx(&full[i], kStageBytes);
-          load_b<FP8>(a, tmB, smB + i * kBBytes, smSF + i * C::kSfBytes, &full[i], nt, sp * a.kb_per_split + i,
-                      kbt, pol_w);
+          load_b<FP8>(a, tmB, smB + i * kBBytes, smSF + i * C::kSfBytes, &full[i], nt, kf + i, kbt, pol_w);
         }
       }
       grid_dependency_wait();     // the gathered rows are written by the gather kernel
@@ -516,10 +543,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the kernel queued after this one (the gate) may start arriving once
         // every CTA has begun its last unit
         if (u + gridDim.x >= a.units) grid_launch_dependents();
-        int mt, nt, sp;
+        int mt, nt, sp, kb0, kbn;
         unit_coords<FUSED>(a, u, mt, nt, sp);
-        const int kb0 = sp * a.kb_per_split;
-        for (int kb = 0; kb < a.kb_per_split; ++kb) {
+        unit_kb(a, u, sp, kb0, kbn);
+        for (int kb = 0; kb < kbn; ++kb) {
           uint8_t* sf = smSF + stage * C::kSfBytes;
           if (u == blockIdx.x && kb < pre) {
             // weight tile already in flight on this stage: add the rows
@@ -566,7 +593,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < a.kb_per_split; ++kb) {
+        int kb_first, kbn;
+        unit_kb(a, u, remainder_unit(a, u) ? static_cast<int>((u - a.full_units) % a.rem_splits)
+                                           : static_cast<int>(u % a.splits),
+                kb_first, kbn);
+        for (int kb = 0; kb < kbn; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -634,7 +665,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       if constexpr (!FUSED) {
-        plain_epilogue(a, t_row, m - lane, nt, sp, lane, smem_u32(epi));
+        if (remainder_unit(a, u)) {
+          // remainder unit j (tile j / rem_splits, K range sp): its fp32 sums go to
+          // the workspace; launch_reduce_remainder adds the ranges up afterwards
+          const int64_t j = u - a.full_units;
+          plain_epilogue(a, t_row, m - lane, nt, sp, lane, smem_u32(epi), a.rem_ws + (j * kBM + q * 32) * kBN, kBN);
+        } else {
+          plain_epilogue(a, t_row, m - lane, nt, sp, lane, smem_u32(epi));
+        }
       } else if (nt < a.key_n_tiles) {
         fused_key_epilogue(a, t_row, m, nt * kBN, lane, reinterpret_cast<float*>(epi));
         fused_key_publish(a, m, mt, q, lane);
@@ -731,6 +769,36 @@ __global__ void __launch_bounds__(256) pack_sfb_kernel(const uint8_t* __restrict
   }
 }
 
+// kv of the remainder tiles: thread (tile, row, lane) adds the tile row's 8
+// columns 8*lane .. over the K ranges in range order and rounds to bf16.
+__global__ void __launch_bounds__(256) reduce_remainder_kernel(const GemmArgs a) {
+  grid_dependency_wait();        // the projection wrote the ranges' sums
+  grid_launch_dependents();
+  const int64_t total = static_cast<int64_t>(a.rem_tiles) * kBM * 32;
+  const int64_t tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
+  const int64_t range_stride = static_cast<int64_t>(kBM) * kBN;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int lane = static_cast<int>(i & 31);
+    const int row = static_cast<int>((i >> 5) % kBM);
+    const int64_t tr = (i >> 5) / kBM;
+    int mt, nt;
+    raster(a, tiles - a.rem_tiles + tr, a.n_tiles, mt, nt);
+    const int64_t m = static_cast<int64_t>(mt) * kBM + row;
+    if (m >= a.M) continue;
+    const float* p = a.rem_ws + (tr * a.rem_splits * kBM + row) * kBN + lane * 8;
+    float4 lo = __ldcg(reinterpret_cast<const float4*>(p)), hi = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    for (int s = 1; s < a.rem_splits; ++s) {
+      const float4* ps = reinterpret_cast<const float4*>(p + s * range_stride);
+      const float4 c = __ldcg(ps), d = __ldcg(ps + 1);
+      lo.x += c.x; lo.y += c.y; lo.z += c.z; lo.w += c.w;
+      hi.x += d.x; hi.y += d.y; hi.z += d.z; hi.w += d.w;
+    }
+    *reinterpret_cast<uint4*>(a.kv + m * a.N + nt * kBN + lane * 8) =
+        make_uint4(pack_bf16x2(lo.x, lo.y), pack_bf16x2(lo.z, lo.w), pack_bf16x2(hi.x, hi.y), pack_bf16x2(hi.z, hi.w));
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -792,6 +860,13 @@ cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* 
   const int64_t blocks = std::min<int64_t>((chunks + 255) / 256, 65536);
   pack_wkv_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(wkv, K, chunks, reinterpret_cast<uint4*>(packed));
   return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_remainder(const GemmArgs& a, int num_sms, cudaStream_t stream) {
+  if (a.rem_splits == 0 || a.rem_tiles == 0) return cudaSuccess;
+  const int64_t total = static_cast<int64_t>(a.rem_tiles) * kBM * 32;
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms) * 8);
+  return launch_pdl(reduce_remainder_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, a);
 }
 
 cudaError_t launch_pack_sfb(const uint8_t* wkv_scale, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream) {

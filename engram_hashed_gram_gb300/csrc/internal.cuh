@@ -83,7 +83,16 @@ struct GemmArgs {
   int32_t m_tiles;
   int32_t n_tiles;
   int32_t group_m;       // m-tiles per rasterisation group
-  int64_t units;         // m_tiles * n_tiles * splits
+  int64_t units;         // full_units + rem_tiles * rem_splits
+  // Remainder split (splits == 1 only): the last rem_tiles tiles of the raster
+  // order, which would otherwise fill only part of a last wave, are cut into
+  // rem_splits K ranges of rem_kb K-blocks; each range stores its fp32 sums in
+  // rem_ws and launch_reduce_remainder adds them up in range order into kv.
+  int64_t full_units;
+  int32_t rem_tiles;
+  int32_t rem_splits;
+  int32_t rem_kb;
+  float* rem_ws;         // [rem_tiles * rem_splits, 128, 256]
   int32_t out_mode;      // GemmOut
   const uint8_t* wpack;  // the weight in tile-packed order (pack_wkv), or nullptr: read through tmB
   int32_t fp8;           // MXFP8 operands: A = table codes [M, K] u8, B = packed weight codes
@@ -132,6 +141,8 @@ cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* 
 // byte 16*l + 4*q + j = scale of K-block j (of 32) of row l + 32*q.  The
 // codes themselves are packed by launch_pack_wkv viewing [N, K] bytes as
 // [N, K/2] 16-bit elements.
+// kv of the remainder tiles from the workspace (after the projection, PDL).
+cudaError_t launch_reduce_remainder(const GemmArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_pack_sfb(const uint8_t* wkv_scale, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream);
 
 // ---- gate and residual (steps a5-a8) ---------------------------------------

@@ -108,7 +108,9 @@ typedef struct {
                            forms the gate and the residual add in the projection's epilogue
                            (kv never reaches HBM) instead of a separate kernel.  Same bits
                            either way; on GB300 the separate kernel measured faster (the
-                           epilogue work slows the power-capped MMA), so 0 is the default. */
+                           epilogue work slows the power-capped MMA), so 0 is the default.
+                           Such a context keeps whole tiles in its plans (no remainder
+                           split, see engram_plan), so that both ways sum kv alike. */
   int32_t wkv_fmt;      /* engram_wkv_fmt; ENGRAM_WKV_MXFP8 needs K a multiple of 128 and
                            takes no fused epilogue (fuse_gate is ignored) */
 } engram_config;
@@ -181,6 +183,11 @@ ENGRAM_API engram_status engram_sync_status(engram_ctx* ctx, engram_stream_t str
 /* Split-K factor and CTA count the projection would use for B*T = m_tokens on
  * this context's device (for tests and benchmarks; queues nothing). */
 ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, int32_t* splits, int32_t* ctas);
+/* (Without split-K, when the tiles fill only part of a last wave of the grid,
+ * the plan also cuts those last tiles into 2-4 K ranges whose fp32 sums are
+ * added in order by the last range to finish; this changes kv's summation
+ * order for those tiles, not its tolerance.  Contexts with max_tokens <= 128
+ * or fuse_gate set keep whole tiles.) */
 
 /* Caps the number of SMs the projection's persistent grid occupies (and that
  * its split-K plan is made for) at `sms`; 0 or more than the device has

@@ -249,7 +249,7 @@ def test_bounded_wait_runs_out_and_the_context_recovers(tiny):
     epilogue never raises its gates-ready flags, the value tiles' bounded wait
     (two seconds) runs out, every role of the projection leaves its loop, and
     engram_sync_status() reports ENGRAM_ETIMEOUT.  The next call on the same
-    context is correct again."""
+    context is correct again (equal to its lookup_project + gate_apply)."""
     import time
     from engram_hashed_gram_gb300 import _lib
     from engram_hashed_gram_gb300.layer import EngramLayer
@@ -270,7 +270,37 @@ def test_bounded_wait_runs_out_and_the_context_recovers(tiny):
         out = fused.forward(ids, x)
         st, _ = fused.sync_status()
         assert st == 0
-        ref = tiny["layer"].forward(ids, x)
+        ref = fused.gate_apply(fused.lookup_project(ids), x)     # the same plan through the separate kernels
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     finally:
         fused.close()
+
+
+def test_remainder_split_tiles(tiny):
+    """1,300 tokens make 11 x 100 = 1,100 output tiles: seven full waves of 152
+    and 36 tiles left over, which the plan cuts into four K ranges each (their
+    fp32 sums reduced in range order by a separate kernel).  Those tiles hold
+    the value columns of every token; sampled tokens are checked against the
+    oracle, and forward equals lookup_project + gate_apply bit for bit."""
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    dev = tiny["dev"]
+    layer = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=1408)
+    try:
+        w, inp = _inputs(tiny, 2, 650, mask_frac=0.05, seed=8)
+        ids, x, mask = _dev(inp)
+        out = layer.forward(ids, x, mask)
+        kv = layer.lookup_project(ids)
+        gates = torch.empty((2, 650, 4), dtype=torch.float32, device="cuda")
+        split = layer.gate_apply(kv, x, mask, gates=gates)
+        assert layer.sync_status()[0] == 0
+        assert layer.plan(1300) == (1, 152)
+        assert torch.equal(out.view(torch.int16), split.view(torch.int16))
+        M = 1300
+        tok = P.sample_tokens(M, 48, np.random.default_rng(8), must=[1279, 1280, 1299])
+        tok_t = torch.from_numpy(tok).cuda()
+        summary = P.check_layer(w, inp, tok, SD.device_bits(out.reshape(M, 4, -1)[tok_t]),
+                                gates.reshape(M, 4)[tok_t].cpu().numpy(), SD.device_bits(kv.reshape(M, -1)[tok_t]),
+                                "remainder split")
+        print(summary)
+    finally:
+        layer.close()
