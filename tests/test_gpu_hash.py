@@ -140,3 +140,24 @@ def test_pipeline_token_ids_to_layer_output(built):
     off = mask.reshape(-1) == 0
     assert np.array_equal(SD.device_bits(out).reshape(w.M, -1)[off], inp.x.reshape(w.M, -1)[off])
     layer.close()
+
+
+def test_full_size_chunked_v41(built):
+    """The full-size workload's shape: B = 2 sessions of 8,192 tokens in four
+    chunks of 2,048, V4.1 layout, with DEAD positions (mask) and ids outside
+    the map; every output id against the oracle."""
+    from engram_hashed_gram_gb300.layer import EngramHasher
+    rng = np.random.default_rng(8192)
+    vocab = 129_280
+    pr = np.array(synth.consecutive_primes_above(16_000_000, 48), dtype=np.int64).reshape(2, 3, 8)
+    token_map, mult, primes, offsets = _params(rng, 2, 4, 8, vocab, primes=pr)
+    B, L = 2, 8192
+    ids = rng.integers(0, vocab, size=(B, L))
+    ids[0, ::997] = vocab + 11
+    mask = (rng.random((B, L)) > 0.02).astype(np.uint8)
+    hasher = EngramHasher(*_dev(token_map, mult, primes, offsets), max_batch=B, max_len=L)
+    cache = np.zeros((B, L), np.int64)
+    for s in range(0, L, 2048):
+        got = hasher(torch.from_numpy(ids[:, s:s + 2048]).cuda(), s, torch.from_numpy(mask[:, s:s + 2048]).cuda())
+        want = H.ngram_hash(ids[:, s:s + 2048], s, cache, token_map, mult, primes, offsets, 2, -1, mask[:, s:s + 2048])
+        assert np.array_equal(got.cpu().numpy(), np.transpose(want, (2, 0, 1, 3))), f"chunk at {s}"
