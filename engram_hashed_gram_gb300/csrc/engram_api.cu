@@ -1,7 +1,10 @@
 // C ABI of the Engram layer (include/engram.h): argument checks, scratch
 // ownership, the projection's work plan and the launch sequence
-//   gather/dequant -> tcgen05 projection -> gate + residual
-// on the caller's stream.  No step runs on the host.
+//   gather/dequant (or, for the MXFP8 weight, gather of codes and scales)
+//   -> tcgen05 projection [-> reduction of remainder-split tiles]
+//   -> gate + residual (from kv, or from the split-K partial sums)
+// on the caller's stream, chained by programmatic dependent launch.  No step
+// runs on the host.
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>

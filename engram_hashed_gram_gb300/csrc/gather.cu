@@ -10,6 +10,9 @@
 // read once with no L1 allocation.  The fp8 -> half conversion is exact and the
 // product is a single fp32 multiply (no FMA contraction), so the result is
 // bit-identical to the definition.
+//
+// gather_codes_kernel serves the MXFP8 weight: it copies the codes unchanged
+// and places the E8M0 scales in the block-scaled projection's order.
 #include "common.cuh"
 #include "internal.cuh"
 

@@ -6,15 +6,19 @@
 //
 // Design (sm_103a, one CTA per SM, persistent):
 //  * a work unit is a 128 x 256 output tile restricted to one K range
-//    (split-K); units are dealt round-robin to the CTAs;
-//  * warp 0 (one thread) streams A = E[A_ROWS rows, 64 k] and B = W[256 rows,
-//    64 k] boxes with TMA (128-byte swizzle) into a STAGES-deep shared-memory
-//    ring;
+//    (split-K, or the remainder split of a small last wave); units are dealt
+//    round-robin to the CTAs;
+//  * warp 0 (one thread) streams A = E[A_ROWS rows, 64 k] with a 2-D TMA copy
+//    (128-byte swizzle) and B = W[256 rows, 64 k] as one contiguous 32 KB bulk
+//    copy of the weight's tile-packed copy (packed at create time exactly as
+//    the swizzled copy would land) into a STAGES-deep shared-memory ring; the
+//    first stages' B copies go out before the wait for the gather;
 //  * warp 1 (one thread) issues tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32)
 //    into one of two 256-column tensor-memory accumulators and commits each
 //    stage back to the producer;
 //  * warps 2-5 drain the other accumulator with tcgen05.ld and write either the
-//    bf16 kv (round to nearest even) or the fp32 partial sums of a K range;
+//    bf16 kv (round to nearest even) or the fp32 partial sums of a K range,
+//    through a per-warp shared-memory tile so that stores are row segments;
 //  * no cluster, no multicast: the L2 serves the reuse of E and W across CTAs.
 // Variants: A_ROWS = 128 with 4 stages in general; for batches of at most 64
 // or 32 tokens the A box holds only 64 or 32 rows, and the shared memory that
