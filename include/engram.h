@@ -110,7 +110,11 @@ typedef struct {
                            either way; on GB300 the separate kernel measured faster (the
                            epilogue work slows the power-capped MMA), so 0 is the default.
                            Such a context keeps whole tiles in its plans (no remainder
-                           split, see engram_plan), so that both ways sum kv alike. */
+                           split, see engram_plan), so that both ways sum kv alike.  The
+                           value tiles wait for gates that other CTAs of the projection
+                           form, which assumes the whole persistent grid is resident at
+                           once: with kernels of other streams holding SMs meanwhile, a
+                           wait may run out (ENGRAM_ETIMEOUT) instead of completing. */
   int32_t wkv_fmt;      /* engram_wkv_fmt; ENGRAM_WKV_MXFP8 needs K a multiple of 128 and
                            takes no fused epilogue (fuse_gate is ignored) */
 } engram_config;
