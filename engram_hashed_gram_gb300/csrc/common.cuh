@@ -230,6 +230,23 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+// Bulk copy shared -> global of `bytes` (16-byte aligned, a multiple of 16),
+// in this thread's bulk group.  The shared data must have been made visible to
+// the async proxy (fence_proxy_async_shared) first.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until this thread's committed bulk stores have read their shared-memory
+// sources (the buffer may be rewritten) / have completed (writes visible).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- block-scaled FP8
 // D[tmem] (+)= (A * sfA) * (B * sfB)^T with e4m3 A and B (K = 32 per
 // instruction) and one E8M0 scale per 32 K per row of A and of B, read from

@@ -186,9 +186,17 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned l
 
 // kv (bf16) or the fp32 split-K partial sums of the warp's 32 rows (m0 ..
 // m0+31), columns [nt*256, nt*256 + 256).  tcgen05.ld gives each lane one
-// row; every 32-column chunk goes through the warp's shared-memory tile so
-// that the global stores are row segments: 8 lanes write one row's 128 bytes
-// of fp32 (4 rows per instruction), or 4 lanes its 64 bytes of bf16 (8 rows).
+// row; every 32-column chunk goes through the warp's shared-memory tile, and
+// from there either
+//  * (a.bulk_epilogue) each lane sends its row's chunk with one bulk copy
+//    (128 bytes of fp32 or 64 of bf16) and never waits on the stores: before
+//    its line is rewritten it waits only for the previous copy to have read
+//    it, and for completion once, at the end of the unit.  Large bf16
+//    batches use this; while the weight streams (decode), or with the MXFP8
+//    operands' many small scale copies, the row copies would queue behind the
+//    loads in the copy engine, so there
+//  * the warp reads the tile back by row segments and stores them (8 lanes
+//    write one row's 128 bytes of fp32, or 4 lanes its 64 bytes of bf16).
 // tile / tile_stride: instead of the output, the fp32 sums go to this 32-row
 // block (row r at tile + r * tile_stride), as for a remainder unit.
 __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m0, int nt, int sp,
@@ -196,12 +204,23 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
                                                int64_t tile_stride = 0) {
   if (m0 >= a.M) return;                             // no row of this quarter is a token
   const bool bf16 = tile == nullptr && a.out_mode == kOutBf16;
+  const uint32_t mine = stage + static_cast<uint32_t>(lane * kPlainPitch);
+  const bool bulk = a.bulk_epilogue != 0;
+  const bool mine_valid = m0 + lane < a.M;
+  uint8_t* row_dst;                                  // bulk mode: this lane's row, first column of the tile
+  if (tile != nullptr) {
+    row_dst = reinterpret_cast<uint8_t*>(tile + lane * tile_stride);
+  } else if (bf16) {
+    row_dst = reinterpret_cast<uint8_t*>(a.kv + (m0 + lane) * a.N + nt * kBN);
+  } else {
+    row_dst = reinterpret_cast<uint8_t*>(a.part + (static_cast<int64_t>(sp) * a.M + m0 + lane) * a.N + nt * kBN);
+  }
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
     tmem_ld_wait();
-    const uint32_t mine = stage + static_cast<uint32_t>(lane * kPlainPitch);
+    if (bulk) bulk_wait_read_all();                  // the previous chunk's copy has left the line
     if (bf16) {
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -213,6 +232,14 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) st_shared_v4(mine + 16 * j, make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
+    }
+    if (bulk) {
+      fence_proxy_async_shared();                    // the line is visible to the bulk copy
+      if (mine_valid) {
+        bulk_store(row_dst + (bf16 ? c * 64 : c * 128), mine, bf16 ? 64u : 128u);
+        bulk_commit();
+      }
+      continue;
     }
     __syncwarp();
     const int n0 = nt * kBN + c * 32;
@@ -241,6 +268,7 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
     }
     __syncwarp();                                    // the tile is rewritten by the next chunk
   }
+  if (bulk) bulk_wait_all();                         // the unit's rows are in global memory
 }
 
 // ---------------------------------------------------------------- fused epilogue
