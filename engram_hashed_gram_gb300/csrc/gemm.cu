@@ -188,7 +188,7 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned l
 // m0+31), columns [nt*256, nt*256 + 256).  tcgen05.ld gives each lane one
 // row; every 32-column chunk goes through the warp's shared-memory tile, and
 // from there either
-//  * (a.bulk_epilogue) each lane sends its row's chunk with one bulk copy
+//  * (BULK, chosen by a.bulk_epilogue) each lane sends its row's chunk with one bulk copy
 //    (128 bytes of fp32 or 64 of bf16) and never waits on the stores: before
 //    its line is rewritten it waits only for the previous copy to have read
 //    it, and for completion once, at the end of the unit.  Large bf16
@@ -199,13 +199,14 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned l
 //    write one row's 128 bytes of fp32, or 4 lanes its 64 bytes of bf16).
 // tile / tile_stride: instead of the output, the fp32 sums go to this 32-row
 // block (row r at tile + r * tile_stride), as for a remainder unit.
+template <bool BULK>
 __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row, int64_t m0, int nt, int sp,
                                                int lane, uint32_t stage, float* tile = nullptr,
                                                int64_t tile_stride = 0) {
   if (m0 >= a.M) return;                             // no row of this quarter is a token
   const bool bf16 = tile == nullptr && a.out_mode == kOutBf16;
   const uint32_t mine = stage + static_cast<uint32_t>(lane * kPlainPitch);
-  const bool bulk = a.bulk_epilogue != 0;
+  constexpr bool bulk = BULK;
   const bool mine_valid = m0 + lane < a.M;
   uint8_t* row_dst;                                  // bulk mode: this lane's row, first column of the tile
   if (tile != nullptr) {
@@ -220,7 +221,7 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
     tmem_ld_wait();
-    if (bulk) bulk_wait_read_all();                  // the previous chunk's copy has left the line
+    if constexpr (bulk) bulk_wait_read_all();        // the previous chunk's copy has left the line
     if (bf16) {
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -233,7 +234,7 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
 #pragma unroll
       for (int j = 0; j < 8; ++j) st_shared_v4(mine + 16 * j, make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
     }
-    if (bulk) {
+    if constexpr (bulk) {
       fence_proxy_async_shared();                    // the line is visible to the bulk copy
       if (mine_valid) {
         bulk_store(row_dst + (bf16 ? c * 64 : c * 128), mine, bf16 ? 64u : 128u);
@@ -268,7 +269,7 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
     }
     __syncwarp();                                    // the tile is rewritten by the next chunk
   }
-  if (bulk) bulk_wait_all();                         // the unit's rows are in global memory
+  if constexpr (bulk) bulk_wait_all();               // the unit's rows are in global memory
 }
 
 // ---------------------------------------------------------------- fused epilogue
@@ -495,7 +496,7 @@ __device__ __forceinline__ bool fused_value_epilogue(const GemmArgs& a, uint32_t
 
 // FUSED selects the gate epilogue at compile time, so that the plain kernel
 // carries none of its registers; FP8 the block-scaled MXFP8 operands.
-template <int A_ROWS, int STAGES, bool FUSED, bool FP8>
+template <int A_ROWS, int STAGES, bool FUSED, bool FP8, bool BULK = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
@@ -701,9 +702,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // remainder unit j (tile j / rem_splits, K range sp): its fp32 sums go to
           // the workspace; launch_reduce_remainder adds the ranges up afterwards
           const int64_t j = u - a.full_units;
-          plain_epilogue(a, t_row, m - lane, nt, sp, lane, smem_u32(epi), a.rem_ws + (j * kBM + q * 32) * kBN, kBN);
+          plain_epilogue<BULK>(a, t_row, m - lane, nt, sp, lane, smem_u32(epi), a.rem_ws + (j * kBM + q * 32) * kBN,
+                               kBN);
         } else {
-          plain_epilogue(a, t_row, m - lane, nt, sp, lane, smem_u32(epi));
+          plain_epilogue<BULK>(a, t_row, m - lane, nt, sp, lane, smem_u32(epi));
         }
       } else if (nt < a.key_n_tiles) {
         fused_key_epilogue(a, t_row, m, nt * kBN, lane, reinterpret_cast<float*>(epi));
@@ -742,6 +744,11 @@ cudaError_t set_smem_attr() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C8::kSmemBytes));
+  if constexpr (A_ROWS == kBM) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(wkv_gemm_kernel<A_ROWS, STAGES, false, false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
+  }
   return e;
 }
 
@@ -754,6 +761,11 @@ cudaError_t launch_variant(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     if (fused || a.wpack == nullptr || a.sfa == nullptr || a.sfb == nullptr) return cudaErrorInvalidConfiguration;
     return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, false, true>, dim3(static_cast<unsigned>(ctas)),
                       dim3(kGemmThreads), Cfg<A_ROWS, STAGES, true>::kSmemBytes, stream, 1, tmA, tmB, a);
+  }
+  if constexpr (A_ROWS == kBM) {                    // bulk-copy epilogue: large bf16 batches only
+    if (!fused && a.bulk_epilogue)
+      return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, false, false, true>, dim3(static_cast<unsigned>(ctas)),
+                        dim3(kGemmThreads), C::kSmemBytes, stream, 1, tmA, tmB, a);
   }
   if (!fused)
     return launch_pdl(wkv_gemm_kernel<A_ROWS, STAGES, false, false>, dim3(static_cast<unsigned>(ctas)),
