@@ -33,6 +33,7 @@ constexpr int kMaxHc = 4;
 constexpr int kBlockCh = 256;                    // channels per reduction block (one warp)
 constexpr int kMaxBlocks = 5120 / kBlockCh;      // blocks per stream for dim = 5120
 constexpr int kGateMaxThreads = kMaxBlocks * 32;
+constexpr int kGateSmallThreads = kMaxBlocks / 4 * 32;   // dim = 5120 in clusters of 4
 
 __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -43,23 +44,55 @@ __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
   }
 }
 
-// 8 kv values from the fp32 partial sums: summed over the splits in order,
-// then rounded to bf16 (the projection's output type).
-__device__ __forceinline__ void load8_partials(const float* part, int splits, int64_t split_stride, float (&f)[8]) {
-  float4 a = __ldg(reinterpret_cast<const float4*>(part));
-  float4 b = __ldg(reinterpret_cast<const float4*>(part) + 1);
-  for (int s = 1; s < splits; ++s) {
-    const float4* p = reinterpret_cast<const float4*>(part + s * split_stride);
-    const float4 c = __ldg(p), d = __ldg(p + 1);
-    a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
-    b.x += d.x; b.y += d.y; b.z += d.z; b.w += d.w;
+// A thread's kv values, 8 per group: group s < HC is stream s's key (offset
+// s * dim), group kMaxHc the value (offset HC * dim), from the fp32 partial
+// sums: summed over the splits in order, then rounded to bf16 (the
+// projection's output type).  The loop runs over splits outside and groups
+// inside, so each split's loads of all groups are in flight together.
+__device__ __forceinline__ bool kv_group(int g, int HC) { return g < HC || g == kMaxHc; }
+__device__ __forceinline__ int kv_offset(int g, int HC, int D) { return (g < kMaxHc ? g : HC) * D; }
+
+__device__ __forceinline__ void load_partials(const float* part, int HC, int D, int splits, int64_t split_stride,
+                                              float (&f)[kMaxHc + 1][8]) {
+#pragma unroll
+  for (int g = 0; g < kMaxHc + 1; ++g) {
+    if (kv_group(g, HC)) {
+      const float4* q = reinterpret_cast<const float4*>(part + kv_offset(g, HC, D));
+      const float4 a = __ldg(q), b = __ldg(q + 1);
+      f[g][0] = a.x; f[g][1] = a.y; f[g][2] = a.z; f[g][3] = a.w;
+      f[g][4] = b.x; f[g][5] = b.y; f[g][6] = b.z; f[g][7] = b.w;
+    }
   }
-  f[0] = round_bf16(a.x); f[1] = round_bf16(a.y); f[2] = round_bf16(a.z); f[3] = round_bf16(a.w);
-  f[4] = round_bf16(b.x); f[5] = round_bf16(b.y); f[6] = round_bf16(b.z); f[7] = round_bf16(b.w);
+  for (int s = 1; s < splits; ++s) {
+    const float* p = part + s * split_stride;
+    float4 c[kMaxHc + 1], d[kMaxHc + 1];
+#pragma unroll
+    for (int g = 0; g < kMaxHc + 1; ++g) {
+      if (kv_group(g, HC)) {
+        const float4* q = reinterpret_cast<const float4*>(p + kv_offset(g, HC, D));
+        c[g] = __ldg(q);
+        d[g] = __ldg(q + 1);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kMaxHc + 1; ++g) {
+      if (kv_group(g, HC)) {
+        f[g][0] += c[g].x; f[g][1] += c[g].y; f[g][2] += c[g].z; f[g][3] += c[g].w;
+        f[g][4] += d[g].x; f[g][5] += d[g].y; f[g][6] += d[g].z; f[g][7] += d[g].w;
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < kMaxHc + 1; ++g)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[g][j] = round_bf16(f[g][j]);
 }
 
-template <bool FROM_PARTIALS>
-__global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const GateArgs a) {
+// MAX_THREADS bounds the block: 160 for dim = 5120 in clusters of 4 (the
+// registers then hold a thread's x, weights and kv at once), kGateMaxThreads
+// for other shapes.
+template <bool FROM_PARTIALS, int MAX_THREADS>
+__global__ void __launch_bounds__(MAX_THREADS) gate_residual_kernel(const GateArgs a) {
   __shared__ float red[kMaxBlocks][3 * kMaxHc];   // every block's sums, pushed by the owning CTAs
   __shared__ float tot[3 * kMaxHc];
   __shared__ float gate_s[kMaxHc];
@@ -91,48 +124,52 @@ __global__ void __launch_bounds__(kGateMaxThreads) gate_residual_kernel(const Ga
     return;
   }
 
-  float h[kMaxHc][8];
+  // the product q_weight * k_weight is formed at create time: it is read
+  // before the wait too
+  float h[kMaxHc][8], w[kMaxHc][8];
 #pragma unroll
-  for (int s = 0; s < kMaxHc; ++s)
-    if (s < HC) unpack8(__ldg(reinterpret_cast<const uint4*>(xm + s * D + d0)), h[s]);
+  for (int s = 0; s < kMaxHc; ++s) {
+    if (s < HC) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(xm + s * D + d0)), h[s]);
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0));
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0) + 1);
+      w[s][0] = w0.x; w[s][1] = w0.y; w[s][2] = w0.z; w[s][3] = w0.w;
+      w[s][4] = w1.x; w[s][5] = w1.y; w[s][6] = w1.z; w[s][7] = w1.w;
+    }
+  }
 
   grid_dependency_wait();        // kv / the partial sums come from the projection
   grid_launch_dependents();
 
-  float v[8];
+  float kv[kMaxHc + 1][8];       // the streams' keys, then the value
+  if (FROM_PARTIALS) {
+    load_partials(a.part + m * N + d0, HC, D, a.splits, a.M * N, kv);
+  } else {
+#pragma unroll
+    for (int g = 0; g < kMaxHc + 1; ++g)
+      if (kv_group(g, HC)) unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + kv_offset(g, HC, D) + d0)), kv[g]);
+  }
   float sums[3 * kMaxHc];
 #pragma unroll
   for (int i = 0; i < 3 * kMaxHc; ++i) sums[i] = 0.0f;
-  const int64_t split_stride = a.M * N;
 #pragma unroll
   for (int s = 0; s < kMaxHc; ++s) {
     if (s < HC) {
-      float k[8];
-      if (FROM_PARTIALS) {
-        load8_partials(a.part + m * N + s * D + d0, a.splits, split_stride, k);
-      } else {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + s * D + d0)), k);
-      }
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0) + 1);
-      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       float sh = 0.0f, sk = 0.0f, sd = 0.0f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         sh = fmaf(h[s][j], h[s][j], sh);
-        sk = fmaf(k[j], k[j], sk);
-        sd = fmaf(__fmul_rn(h[s][j], w[j]), k[j], sd);
+        sk = fmaf(kv[s][j], kv[s][j], sk);
+        sd = fmaf(__fmul_rn(h[s][j], w[s][j]), kv[s][j], sd);
       }
       sums[3 * s + 0] = sh;
       sums[3 * s + 1] = sk;
       sums[3 * s + 2] = sd;
     }
   }
-  if (FROM_PARTIALS) {
-    load8_partials(a.part + m * N + static_cast<int64_t>(HC) * D + d0, a.splits, split_stride, v);
-  } else {
-    unpack8(__ldg(reinterpret_cast<const uint4*>(a.kv + m * N + static_cast<int64_t>(HC) * D + d0)), v);
-  }
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = kv[kMaxHc][j];
 
   // one block sum per warp: xor butterfly 16, 8, 4, 2, 1
 #pragma unroll
@@ -373,8 +410,14 @@ cudaError_t launch_gate(const GateArgs& a_in, cudaStream_t stream) {
   a.cluster = gate_cluster_size(a.dim);
   const unsigned threads = static_cast<unsigned>(a.dim / kBlockCh / a.cluster * 32);
   const dim3 grid(static_cast<unsigned>(a.M * a.cluster));
-  if (a.part != nullptr) return launch_pdl(gate_residual_kernel<true>, grid, dim3(threads), 0, stream, a.cluster, a);
-  return launch_pdl(gate_residual_kernel<false>, grid, dim3(threads), 0, stream, a.cluster, a);
+  if (threads <= kGateSmallThreads) {
+    if (a.part != nullptr)
+      return launch_pdl(gate_residual_kernel<true, kGateSmallThreads>, grid, dim3(threads), 0, stream, a.cluster, a);
+    return launch_pdl(gate_residual_kernel<false, kGateSmallThreads>, grid, dim3(threads), 0, stream, a.cluster, a);
+  }
+  if (a.part != nullptr)
+    return launch_pdl(gate_residual_kernel<true, kGateMaxThreads>, grid, dim3(threads), 0, stream, a.cluster, a);
+  return launch_pdl(gate_residual_kernel<false, kGateMaxThreads>, grid, dim3(threads), 0, stream, a.cluster, a);
 }
 
 cudaError_t launch_reduce_partials(const float* part, int32_t splits, int64_t M, int32_t N, uint16_t* kv,
