@@ -66,6 +66,7 @@ struct Plan {
 
 constexpr int kMaxRemSplits = 4;
 constexpr int64_t kBulkEpilogueTokens = 2048;
+constexpr int64_t kKeepWeightTokens = 2048;
 
 Plan make_plan(const engram_ctx* c, int64_t M) {
   Plan p{};
@@ -228,6 +229,12 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
   // weight streams (decode, 512 tokens) or in the MXFP8 kernel (4,096 tokens:
   // 614 -> 757 us), where the copies queue with the many small scale loads
   a.bulk_epilogue = !c->fp8 && M >= kBulkEpilogueTokens ? 1 : 0;
+  // a weight tile is read by every M tile of a 16-tile group; from 16 M tiles
+  // on, those reads drift apart in time and an evict-first tile is often gone
+  // before the last of them (measured on GB300, evict-last: 4,096 tokens
+  // 886 -> 857 us, MXFP8 610 -> 587 us, 16,384 tokens 3.77 -> 3.50 ms; at 512
+  // tokens, 4 M tiles in step, it cost 134 -> 140 us)
+  a.keep_weight = M >= kKeepWeightTokens ? 1 : 0;
   a.fp8 = c->fp8 ? 1 : 0;
   a.sfa = c->sfa;
   a.sfb = c->wsf;

@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_w = a.keep_weight ? policy_evict_last() : policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued[kStages] = {};

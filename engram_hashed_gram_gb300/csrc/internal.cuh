@@ -95,6 +95,7 @@ struct GemmArgs {
   float* rem_ws;         // [rem_tiles * rem_splits, 128, 256]
   int32_t out_mode;      // GemmOut
   int32_t bulk_epilogue; // plain epilogue stores by per-row bulk copies (large batches)
+  int32_t keep_weight;   // weight tiles L2 evict-last (shared by many M tiles) instead of evict-first
   const uint8_t* wpack;  // the weight in tile-packed order (pack_wkv), or nullptr: read through tmB
   int32_t fp8;           // MXFP8 operands: A = table codes [M, K] u8, B = packed weight codes
   const uint8_t* sfa;    // fp8: A scales, [m_tiles, K/128, 512] (gather_codes layout)
