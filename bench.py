@@ -261,6 +261,8 @@ def config_of(w):
             "prime_base": w.prime_base,
             "wkv": "bf16 [25600, 6144]" if w.wkv_fmt == 0 else "mxfp8 [25600, 6144]: e4m3 + e8m0 per 32 inputs",
             "table_scales": "fp32 per 128" if w.scale_fmt == 0 else "e8m0 per 32", "fuse_gate": bool(getattr(ARGS, "fuse_gate", False)),
+            "table_placement": ("pinned host memory, read in place over the host link"
+                                if getattr(ARGS, "table_host", False) else "device"),
             "l2": L2_NOTE}
 
 
@@ -278,9 +280,10 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.set_device(dev)
     M = w.M
     inp = synth.make_inputs(w)
-    table, scale = SD.make_table(w, device=dev)
+    table, scale = SD.make_table(w, device=dev, host=args.table_host)
     d = SD.upload_inputs(inp, device=dev)
     layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps, fuse_gate=args.fuse_gate,
+                        device=dev,
                         scale_block=w.scale_block, scale_fmt=w.scale_fmt, wkv_scale=d["wkv_scale"])
     ids, x, mask = d["hash_ids"], d["x"], d["mask"]
     out = torch.empty_like(x)
@@ -568,11 +571,11 @@ def run_runahead(args, w):
     dev = torch.device("cuda", 0)
     M = w.M
     inp = synth.make_inputs(w)
-    table, scale = SD.make_table(w)
+    table, scale = SD.make_table(w, host=args.table_host)
     d = SD.upload_inputs(inp)
     w2 = dataclasses.replace(w, seed=w.seed + 100)
     wkv2 = SD.bits_to_device(synth.make_wkv(w2)) if w.wkv_fmt == 0 else None
-    kw = dict(max_tokens=M, eps=w.eps, scale_block=w.scale_block, scale_fmt=w.scale_fmt)
+    kw = dict(max_tokens=M, eps=w.eps, scale_block=w.scale_block, scale_fmt=w.scale_fmt, device=dev)
     if w.wkv_fmt == 0:
         layers = [EngramLayer(table, scale, d["wkv"], d["q"], d["k"], **kw),
                   EngramLayer(table, scale, wkv2, d["q"], d["k"], **kw)]
@@ -667,6 +670,7 @@ def run_runahead(args, w):
             "config": {"workload": w.name, "B": w.B, "T": w.T, "engram_layers": [1, 14],
                        "engram_sm_budget": budgets, "engram_plan_runahead": ra_plan,
                        "backbone_stand_in": f"15 x bf16 [{4 * M}, {w.dim}] x [{w.dim}, {w.dim}] matmul",
+                       "table_placement": "pinned host memory" if args.table_host else "device",
                        "l2": L2_NOTE}}
 
 
@@ -686,6 +690,9 @@ def main():
     ap.add_argument("--sm-budget", default=None,
                     help="runahead: cap the Engram projections at this many SMs (engram_set_sm_budget): one "
                          "count, or one per layer separated by commas (0 = all SMs)")
+    ap.add_argument("--table-host", action="store_true",
+                    help="keep the table and its scales in pinned host memory (the gather reads them over the "
+                         "host link)")
     ap.add_argument("--fuse-gate", action="store_true",
                     help="form the gate in the projection's epilogue (engram_config.fuse_gate)")
     ap.add_argument("--prime-base", type=int, default=None,

@@ -54,6 +54,22 @@ constexpr int64_t kSplitMaxTokens = 128;   // split-K only while one M tile cove
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Whether kernels on `device` can read p at address p: memory of that device,
+// managed memory, or pinned host memory mapped at the same address.
+bool device_readable(const void* p, int device) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: return at.device == device;
+    case cudaMemoryTypeManaged: return true;
+    case cudaMemoryTypeHost: return at.devicePointer == p;
+    default: return false;
+  }
+}
+
 struct Plan {
   int32_t splits;
   int32_t ctas;
@@ -357,6 +373,10 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
       cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
     delete ctx;
     return ENGRAM_ECUDA;
+  }
+  if (!device_readable(w->table, ctx->device) || !device_readable(w->scale, ctx->device)) {
+    delete ctx;
+    return ENGRAM_EINVAL;
   }
   int cc_major = 0, cc_minor = 0;
   cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, ctx->device);

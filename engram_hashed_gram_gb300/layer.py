@@ -50,18 +50,29 @@ class EngramLayer:
     n_cols*head_dim], or its uint8 e4m3 codes together with wkv_scale (uint8
     E8M0 [dim*(hc+1), n_cols*head_dim/32]) for the MXFP8 weight; q_weight,
     k_weight: bf16 [hc, dim].  The tensors are referenced, not copied, and are
-    kept alive by this object."""
+    kept alive by this object.  table and scale may instead be pinned host
+    tensors (``pin_memory()``): the gather then reads them in place over the
+    host link, the layer runs on ``device`` (default: the current CUDA
+    device)."""
 
     def __init__(self, table, scale, wkv, q_weight, k_weight, *, dim=5120, hc_mult=4, n_cols=24, head_dim=256,
                  scale_block=128, scale_fmt=_lib.SCALE_F32, eps=1e-6, clamp=1e-6, max_tokens=4096,
-                 check_ids=False, fuse_gate=False, wkv_scale=None):
-        dev = table.device
+                 check_ids=False, fuse_gate=False, wkv_scale=None, device=None):
+        if table.device.type == "cuda":
+            dev = table.device
+        elif table.is_pinned():
+            dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        else:
+            raise ValueError("table must be a CUDA tensor or a pinned host tensor")
         if dev.type != "cuda":
             raise ValueError("the Engram layer runs on a CUDA device only")
         R = table.shape[0]
-        _need(table, "table", (torch.uint8,), (R, head_dim), dev)
+        tdev = table.device
+        if tdev.type != "cuda" and not (scale.device.type == "cpu" and scale.is_pinned()):
+            raise ValueError("with a pinned host table, scale must be pinned host memory too")
+        _need(table, "table", (torch.uint8,), (R, head_dim), tdev)
         _need(scale, "scale", (torch.float32,) if scale_fmt == _lib.SCALE_F32 else (torch.uint8,),
-              (R, head_dim // scale_block), dev)
+              (R, head_dim // scale_block), tdev)
         wkv_fmt = _lib.WKV_BF16 if wkv_scale is None else _lib.WKV_MXFP8
         if wkv_fmt == _lib.WKV_BF16:
             _need(wkv, "wkv", _U16, (dim * (hc_mult + 1), n_cols * head_dim), dev)

@@ -14,6 +14,16 @@ def _check(rc: int, where: str) -> None:
         raise RuntimeError(f"{where} failed with {rc}")
 
 
+def _cuda_device(t: torch.Tensor) -> torch.device:
+    """The device whose kernels fill t: its own, or the current CUDA device for
+    a pinned host tensor (written in place over the host link)."""
+    if t.is_cuda:
+        return t.device
+    if not t.is_pinned():
+        raise ValueError("a host tensor filled by the device generator must be pinned")
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def fill_table(table: torch.Tensor, scale: torch.Tensor | None, seed: int, scale_block: int = 128,
                row_begin: int = 0, row_end: int | None = None, stream=None) -> None:
     """Writes rows [row_begin, row_end) of a uint8 [R, head_dim] table and its
@@ -21,7 +31,7 @@ def fill_table(table: torch.Tensor, scale: torch.Tensor | None, seed: int, scale
     lib = _lib.synth()
     R, head_dim = table.shape
     row_end = R if row_end is None else row_end
-    dev = table.device
+    dev = _cuda_device(table)
     cq = torch.from_numpy(synth.code_quantile_table().copy()).to(dev)
     sq = torch.from_numpy(synth.scale_quantile_table().copy()).to(dev)
     st = torch.cuda.current_stream(dev).cuda_stream if stream is None else int(stream)
@@ -40,7 +50,7 @@ def fill_scales_e8m0(scale: torch.Tensor, seed: int, head_dim: int, scale_block:
     synth.table_rows(seed, ..., scale_fmt=1)."""
     lib = _lib.synth()
     R = scale.shape[0]
-    dev = scale.device
+    dev = _cuda_device(scale)
     eq = torch.from_numpy(synth.e8m0_quantile_table().copy()).to(dev)
     st = torch.cuda.current_stream(dev).cuda_stream if stream is None else int(stream)
     _check(lib.engram_synth_fill_scales_e8m0(scale.data_ptr(), 0, R, head_dim, scale_block,
@@ -49,18 +59,23 @@ def fill_scales_e8m0(scale: torch.Tensor, seed: int, head_dim: int, scale_block:
     torch.cuda.current_stream(dev).synchronize()
 
 
-def make_table(w: synth.Workload, device="cuda", num_rows: int | None = None):
+def make_table(w: synth.Workload, device="cuda", num_rows: int | None = None, host: bool = False):
     """(table uint8 [R, head_dim], scales [R, head_dim/scale_block]) on the
-    device: fp32 scales, or E8M0 bytes for the mxfp8 format."""
+    device, or in pinned host memory with host=True (filled in place by the
+    device generator): fp32 scales, or E8M0 bytes for the mxfp8 format."""
     R = w.num_rows() if num_rows is None else num_rows
-    table = torch.empty((R, w.head_dim), dtype=torch.uint8, device=device)
     nb = w.head_dim // w.scale_block
+    sdt = torch.uint8 if w.scale_fmt == 1 else torch.float32
+    if host:
+        table = torch.empty((R, w.head_dim), dtype=torch.uint8, pin_memory=True)
+        scale = torch.empty((R, nb), dtype=sdt, pin_memory=True)
+    else:
+        table = torch.empty((R, w.head_dim), dtype=torch.uint8, device=device)
+        scale = torch.empty((R, nb), dtype=sdt, device=device)
     if w.scale_fmt == 1:
         fill_table(table, None, w.seed, w.scale_block)
-        scale = torch.empty((R, nb), dtype=torch.uint8, device=device)
         fill_scales_e8m0(scale, w.seed, w.head_dim, w.scale_block)
     else:
-        scale = torch.empty((R, nb), dtype=torch.float32, device=device)
         fill_table(table, scale, w.seed, w.scale_block)
     return table, scale
 

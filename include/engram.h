@@ -119,9 +119,18 @@ typedef struct {
                            takes no fused epilogue (fuse_gate is ignored) */
 } engram_config;
 
+/* table and scale may live in device memory or in host memory that the device
+ * reads in place: pinned host memory (cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped) whose device address equals its host address, as it
+ * does under unified addressing.  A host-resident table is gathered by the
+ * same kernel, its rows crossing the host link on every call (NVLink-C2C on a
+ * Grace-Blackwell node): the pages keep the tables in host memory.  engram_create
+ * returns ENGRAM_EINVAL for a table or scale pointer the device cannot read at
+ * that address (unregistered host memory, another device's memory). */
 typedef struct {
-  const uint8_t* table;     /* device, [R, head_dim] fp8-e4m3 codes */
-  const void* scale;        /* device, [R, head_dim/scale_block] fp32 or uint8 E8M0 */
+  const uint8_t* table;     /* device or mapped pinned host, [R, head_dim] fp8-e4m3 codes */
+  const void* scale;        /* device or mapped pinned host, [R, head_dim/scale_block]
+                               fp32 or uint8 E8M0 */
   const void* wkv;          /* device, [dim*(hc_mult+1), n_cols*head_dim], the Linear's
                                [out, in] weight: keys of stream s at rows s*dim ..
                                s*dim+dim-1, the value at rows hc_mult*dim ..; bf16 bits

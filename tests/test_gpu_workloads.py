@@ -5,6 +5,8 @@ the benchmark times (one engram_forward over the whole batch):
   prefill_1x4096_zipf  B=1,    T=4096, 402,659,764 rows (103 GB), Zipf ids, 10% masked span
   decode_512x1_skew    B=512,  T=1,    100,667,472 rows (25.8 GB), hot-set ids, near-zero streams
   full_2x8192          B=2,    T=8192, 384,016,682 rows (98.3 GB), 5% masked
+  decode_64x1_mxfp8, prefill_1x4096_mxfp8: the decode and prefill shapes with
+                       the MXFP8 table (E8M0 per 32) and the MXFP8 weight
 
 The table is filled on the device by the generator's twin; the oracle
 regenerates only the rows of the sampled tokens.  Sampled tokens are checked
@@ -22,7 +24,8 @@ import parity as P
 
 pytestmark = pytest.mark.gpu
 
-WORKLOADS = ["decode_64x1", "prefill_1x4096_zipf", "decode_512x1_skew", "full_2x8192"]
+WORKLOADS = ["decode_64x1", "prefill_1x4096_zipf", "decode_512x1_skew", "full_2x8192", "decode_64x1_mxfp8",
+             "prefill_1x4096_mxfp8"]
 
 
 @pytest.mark.parametrize("name", WORKLOADS)
@@ -37,7 +40,8 @@ def test_workload_parity(name):
     inp = synth.make_inputs(w)
     table, scale = SD.make_table(w)
     d = SD.upload_inputs(inp)
-    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps)
+    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps, scale_block=w.scale_block,
+                        scale_fmt=w.scale_fmt, wkv_scale=d["wkv_scale"])
     try:
         ids, x, mask = d["hash_ids"], d["x"], d["mask"]
         out = layer.forward(ids, x, mask)
