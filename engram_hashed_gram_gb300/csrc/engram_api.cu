@@ -293,6 +293,8 @@ GateArgs gate_args(const engram_ctx* c, const uint16_t* x, const uint8_t* mask, 
   a.eps = c->cfg.eps;
   a.clamp = c->cfg.clamp;
   a.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c->cfg.dim)));
+  a.err = c->err;
+  a.num_sms = c->num_sms;
   return a;
 }
 
@@ -420,7 +422,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
                  launch_pack_sfb(w->wkv_scale, N, K, ctx->wsf, nullptr) != cudaSuccess ||
                  cudaMemset(ctx->sfa, 127, sfa_bytes) != cudaSuccess   // scales of rows past M: 1.0
            : launch_pack_wkv(static_cast<const uint16_t*>(w->wkv), N, K, ctx->wpack, nullptr) != cudaSuccess) ||
-      gemm_prepare() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      gemm_prepare() != cudaSuccess || gate_prepare() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     free_ctx(ctx);
     return ENGRAM_ECUDA;
   }

@@ -224,128 +224,166 @@ __global__ void __launch_bounds__(MAX_THREADS) gate_residual_kernel(const GateAr
   }
 }
 
-// The same layer step for large batches: one CTA per token and no cluster.
-// Warp w owns blocks w*BPW .. w*BPW+BPW-1 of every stream (lane l channels
-// 8l..8l+7 of each), so the per-block sums, the butterflies and the block
-// order are exactly those of gate_residual_kernel and the two give the same
-// bits.  Every load of the token (x, key and value, 16 bytes each) is issued
-// before any arithmetic, so a CTA keeps (2 HC + 1) * BPW * 16 bytes per thread
-// in flight; with two CTAs per SM that covers HBM latency.  kv only (no
-// split-K partials: large batches do not split K).
+// The same layer step for bf16 kv as a persistent streaming kernel: one CTA
+// per SM walks the tokens blockIdx.x, blockIdx.x + gridDim.x, ...; thread 0
+// fetches each token's x and kv rows (contiguous: 40 KB and 50 KB at dim =
+// 5120, hc = 4) with two bulk copies into a two-slot shared-memory ring, so
+// the next token streams in while this one is gated, and q_weight*k_weight is
+// read once per CTA.  Warp w owns blocks w*BPW .. w*BPW+BPW-1 of every stream
+// and lane l channels 8l..8l+7 of each, so every block's sums are formed by
+// the same lane and warp arithmetic as in gate_residual_kernel, and the block
+// sums are added in the same order: the same bits.
 template <int BPW>
-__global__ void __launch_bounds__(kMaxBlocks / BPW * 32, 2) gate_residual_wide_kernel(const GateArgs a) {
+__global__ void __launch_bounds__(kMaxBlocks / BPW * 32, 1) gate_residual_stream_kernel(const GateArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[2];
   __shared__ float red[kMaxBlocks][3 * kMaxHc];
   __shared__ float tot[3 * kMaxHc];
   __shared__ float gate_s[kMaxHc];
+  __shared__ int abort_flag;
 
-  const int64_t m = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int D = a.dim;
   const int HC = a.hc;
   const int nblocks = D / kBlockCh;
   const int64_t N = static_cast<int64_t>(D) * (HC + 1);
-  const uint16_t* xm = a.x + m * HC * D;
-  uint16_t* om = a.out + m * HC * D;
+  const uint32_t xbytes = static_cast<uint32_t>(HC * D * 2);
+  const uint32_t kvbytes = static_cast<uint32_t>(N * 2);
+  const uint32_t slot = (xbytes + kvbytes + 127u) & ~127u;
   int d0[BPW];
 #pragma unroll
   for (int j = 0; j < BPW; ++j) d0[j] = (warp * BPW + j) * kBlockCh + lane * 8;
 
-  if (a.mask != nullptr && a.mask[m] == 0) {
-    grid_dependency_wait();
-    if (om != xm) {
-#pragma unroll
-      for (int j = 0; j < BPW; ++j)
-        for (int s = 0; s < HC; ++s)
-          *reinterpret_cast<uint4*>(om + s * D + d0[j]) = __ldg(reinterpret_cast<const uint4*>(xm + s * D + d0[j]));
-    }
-    if (a.gates != nullptr && threadIdx.x < HC) a.gates[m * HC + threadIdx.x] = 0.0f;
-    grid_launch_dependents();
-    return;
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbarrier_init();
+    abort_flag = 0;
   }
-
-  uint4 xr[BPW][kMaxHc], kr[BPW][kMaxHc], vr[BPW];
+  // q_weight * k_weight, formed at create time, once per CTA
+  float w[BPW][kMaxHc][8];
 #pragma unroll
   for (int j = 0; j < BPW; ++j)
 #pragma unroll
     for (int s = 0; s < kMaxHc; ++s)
-      if (s < HC) xr[j][s] = __ldg(reinterpret_cast<const uint4*>(xm + s * D + d0[j]));
-  grid_dependency_wait();        // kv comes from the projection
-  grid_launch_dependents();
-  const uint16_t* kvm = a.kv + m * N;
-#pragma unroll
-  for (int j = 0; j < BPW; ++j) {
-#pragma unroll
-    for (int s = 0; s < kMaxHc; ++s)
-      if (s < HC) kr[j][s] = __ldg(reinterpret_cast<const uint4*>(kvm + s * D + d0[j]));
-    vr[j] = __ldg(reinterpret_cast<const uint4*>(kvm + static_cast<int64_t>(HC) * D + d0[j]));
-  }
-
-#pragma unroll
-  for (int j = 0; j < BPW; ++j) {
-    float sums[3 * kMaxHc];
-#pragma unroll
-    for (int s = 0; s < kMaxHc; ++s) {
-      sums[3 * s] = sums[3 * s + 1] = sums[3 * s + 2] = 0.0f;
       if (s < HC) {
-        float h[8], k[8];
-        unpack8(xr[j][s], h);
-        unpack8(kr[j][s], k);
         const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0[j]));
         const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0[j]) + 1);
-        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        float sh = 0.0f, sk = 0.0f, sd = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          sh = fmaf(h[c], h[c], sh);
-          sk = fmaf(k[c], k[c], sk);
-          sd = fmaf(__fmul_rn(h[c], w[c]), k[c], sd);
-        }
-        sums[3 * s] = sh;
-        sums[3 * s + 1] = sk;
-        sums[3 * s + 2] = sd;
+        w[j][s][0] = w0.x; w[j][s][1] = w0.y; w[j][s][2] = w0.z; w[j][s][3] = w0.w;
+        w[j][s][4] = w1.x; w[j][s][5] = w1.y; w[j][s][6] = w1.z; w[j][s][7] = w1.w;
       }
-    }
-#pragma unroll
-    for (int i = 0; i < 3 * kMaxHc; ++i) {
-      float v = sums[i];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-      if (lane == 0) red[warp * BPW + j][i] = v;
-    }
-  }
   __syncthreads();
-  if (threadIdx.x < 3 * HC) {            // one (stream, quantity) per thread, blocks in order
-    float acc = 0.0f;
-    for (int b = 0; b < nblocks; ++b) acc += red[b][threadIdx.x];
-    tot[threadIdx.x] = acc;
-  }
-  __syncthreads();
-  if (threadIdx.x < HC) {
-    const int t = threadIdx.x;
-    const float g = engram_gate(tot[3 * t], tot[3 * t + 1], tot[3 * t + 2], D, a.eps, a.clamp, a.inv_sqrt_dim);
-    gate_s[t] = g;
-    if (a.gates != nullptr) a.gates[m * HC + t] = g;
-  }
-  __syncthreads();
+  grid_dependency_wait();        // kv comes from the projection
+  grid_launch_dependents();
 
+  const uint64_t pol = policy_evict_first();
+  const int64_t step = gridDim.x;
+  uint32_t issued[2] = {0u, 0u};   // thread 0: copies issued per slot
+  auto fetch = [&](int64_t m, int b) {
+    uint8_t* xs = ring + b * slot;
+    mbar_arrive_expect_tx(&full[b], xbytes + kvbytes);
+    bulk_load_hint(xs, a.x + m * HC * D, xbytes, &full[b], pol);
+    bulk_load_hint(xs + xbytes, a.kv + m * N, kvbytes, &full[b], pol);
+    ++issued[b];
+  };
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b)
+      if (blockIdx.x + b * step < a.M) fetch(blockIdx.x + b * step, b);
+  }
+
+  int i = 0;
+  for (int64_t m = blockIdx.x; m < a.M; m += step, ++i) {
+    const int b = i & 1;
+    const bool ok = mbar_wait(&full[b], static_cast<uint32_t>((i >> 1) & 1), &abort_flag);
+    if (!ok && threadIdx.x == 0) {
+      abort_flag = 1;
+      atomicOr(a.err, kErrTimeout);
+    }
+    __syncthreads();
+    if (abort_flag) break;
+    const uint32_t xs = smem_u32(ring + b * slot);
+    const uint32_t ks = xs + xbytes;
+    uint16_t* om = a.out + m * HC * D;
+
+    if (a.mask != nullptr && a.mask[m] == 0) {
+      // "pass through untouched": the streams are copied, the gate is 0
 #pragma unroll
-  for (int j = 0; j < BPW; ++j) {
-    float v[8];
-    unpack8(vr[j], v);
+      for (int j = 0; j < BPW; ++j)
+        for (int s = 0; s < HC; ++s)
+          *reinterpret_cast<uint4*>(om + s * D + d0[j]) = ld_shared_v4(xs + 2u * static_cast<uint32_t>(s * D + d0[j]));
+      if (a.gates != nullptr && threadIdx.x < HC) a.gates[m * HC + threadIdx.x] = 0.0f;
+    } else {
 #pragma unroll
-    for (int s = 0; s < kMaxHc; ++s) {
-      if (s < HC) {
-        const float g = gate_s[s];
-        float h[8];
-        unpack8(xr[j][s], h);
-        uint4 o;
-        o.x = pack_bf16x2(fmaf(g, v[0], h[0]), fmaf(g, v[1], h[1]));
-        o.y = pack_bf16x2(fmaf(g, v[2], h[2]), fmaf(g, v[3], h[3]));
-        o.z = pack_bf16x2(fmaf(g, v[4], h[4]), fmaf(g, v[5], h[5]));
-        o.w = pack_bf16x2(fmaf(g, v[6], h[6]), fmaf(g, v[7], h[7]));
-        *reinterpret_cast<uint4*>(om + s * D + d0[j]) = o;
+      for (int j = 0; j < BPW; ++j) {
+        float sums[3 * kMaxHc];
+#pragma unroll
+        for (int s = 0; s < kMaxHc; ++s) {
+          sums[3 * s] = sums[3 * s + 1] = sums[3 * s + 2] = 0.0f;
+          if (s < HC) {
+            float h[8], k[8];
+            unpack8(ld_shared_v4(xs + 2u * static_cast<uint32_t>(s * D + d0[j])), h);
+            unpack8(ld_shared_v4(ks + 2u * static_cast<uint32_t>(s * D + d0[j])), k);
+            float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              sh = fmaf(h[c], h[c], sh);
+              sk = fmaf(k[c], k[c], sk);
+              sd = fmaf(__fmul_rn(h[c], w[j][s][c]), k[c], sd);
+            }
+            sums[3 * s] = sh;
+            sums[3 * s + 1] = sk;
+            sums[3 * s + 2] = sd;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 3 * kMaxHc; ++q) {
+          float v = sums[q];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+          if (lane == 0) red[warp * BPW + j][q] = v;
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x < 3 * HC) {        // one (stream, quantity) per thread, blocks in order
+        float acc = 0.0f;
+        for (int blk = 0; blk < nblocks; ++blk) acc += red[blk][threadIdx.x];
+        tot[threadIdx.x] = acc;
+      }
+      __syncthreads();
+      if (threadIdx.x < HC) {
+        const int t = threadIdx.x;
+        const float g = engram_gate(tot[3 * t], tot[3 * t + 1], tot[3 * t + 2], D, a.eps, a.clamp, a.inv_sqrt_dim);
+        gate_s[t] = g;
+        if (a.gates != nullptr) a.gates[m * HC + t] = g;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < BPW; ++j) {
+        float v[8];
+        unpack8(ld_shared_v4(ks + 2u * static_cast<uint32_t>(HC * D + d0[j])), v);
+#pragma unroll
+        for (int s = 0; s < kMaxHc; ++s) {
+          if (s < HC) {
+            const float g = gate_s[s];
+            float h[8];
+            unpack8(ld_shared_v4(xs + 2u * static_cast<uint32_t>(s * D + d0[j])), h);
+            uint4 o;
+            o.x = pack_bf16x2(fmaf(g, v[0], h[0]), fmaf(g, v[1], h[1]));
+            o.y = pack_bf16x2(fmaf(g, v[2], h[2]), fmaf(g, v[3], h[3]));
+            o.z = pack_bf16x2(fmaf(g, v[4], h[4]), fmaf(g, v[5], h[5]));
+            o.w = pack_bf16x2(fmaf(g, v[6], h[6]), fmaf(g, v[7], h[7]));
+            *reinterpret_cast<uint4*>(om + s * D + d0[j]) = o;
+          }
+        }
       }
     }
+    __syncthreads();                     // slot b and gate_s are free again
+    if (threadIdx.x == 0 && m + 2 * step < a.M) fetch(m + 2 * step, b);
+  }
+  if (threadIdx.x == 0 && abort_flag) {
+    // let every copy already issued land before the CTA can exit
+    for (int b = 0; b < 2; ++b)
+      if (issued[b] > 0) mbar_wait(&full[b], (issued[b] - 1u) & 1u, nullptr, kDrainLimitNs);
   }
 }
 
@@ -382,30 +420,48 @@ int gate_cluster_size(int dim) {
   return nblocks % 4 == 0 ? 4 : (nblocks % 2 == 0 ? 2 : 1);
 }
 
-// Batches of at least this many tokens (with bf16 kv) take the one-CTA-per-
-// token kernel; smaller ones spread each token over a cluster for latency
-// (measured on GB300: 512 tokens 25.3 -> 20.5 us, 4096 tokens 167 -> 98 us,
-// 16384 tokens 688 -> 378 us).  ENGRAM_GATE_WIDE_MIN overrides it for
-// measurements.
-int64_t gate_wide_min_tokens() {
+// Shared memory of the streaming kernel: two slots of one token's x and kv.
+size_t gate_stream_smem(int dim, int hc) {
+  const size_t slot = (static_cast<size_t>(hc) * dim * 2 + static_cast<size_t>(hc + 1) * dim * 2 + 127) & ~size_t{127};
+  return 2 * slot;
+}
+
+// Batches of at least this many tokens (with bf16 kv) take the streaming
+// kernel, smaller ones spread each token over a cluster for latency.  Measured
+// on GB300 inside a layer step against the one-CTA-per-token kernel it
+// replaced: 512 tokens 137.6 -> 136.0 us, 4,096 tokens 862 -> 844 us, 16,384
+// tokens 3.35 -> 3.27 ms (that kernel in turn had taken 512 tokens from 25.3 to
+// 20.5 us, 4,096 tokens from 167 to 98 us against the cluster kernel).
+// ENGRAM_GATE_STREAM_MIN overrides the threshold for measurements.
+int64_t gate_stream_min_tokens() {
   static const int64_t v = [] {
-    const char* e = std::getenv("ENGRAM_GATE_WIDE_MIN");
+    const char* e = std::getenv("ENGRAM_GATE_STREAM_MIN");
     return e != nullptr ? static_cast<int64_t>(std::atoll(e)) : int64_t{256};
   }();
   return v;
+}
+
+cudaError_t gate_prepare() {
+  const int smem = static_cast<int>(gate_stream_smem(5120, kMaxHc));
+  cudaError_t e = cudaFuncSetAttribute(gate_residual_stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gate_residual_stream_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
 }
 
 cudaError_t launch_gate(const GateArgs& a_in, cudaStream_t stream) {
   if (a_in.M == 0) return cudaSuccess;
   GateArgs a = a_in;
   const int nblocks = a.dim / kBlockCh;
-  if (a.part == nullptr && a.M >= gate_wide_min_tokens()) {
+  if (a.part == nullptr && a.err != nullptr && a.num_sms > 0 && a.M >= gate_stream_min_tokens()) {
     a.cluster = 1;
-    const dim3 grid(static_cast<unsigned>(a.M));
+    const size_t smem = gate_stream_smem(a.dim, a.hc);
+    const dim3 grid(static_cast<unsigned>(a.M < a.num_sms ? a.M : a.num_sms));
     if (nblocks % 2 == 0)
-      return launch_pdl(gate_residual_wide_kernel<2>, grid, dim3(static_cast<unsigned>(nblocks / 2 * 32)), 0, stream,
-                        1, a);
-    return launch_pdl(gate_residual_wide_kernel<1>, grid, dim3(static_cast<unsigned>(nblocks * 32)), 0, stream, 1, a);
+      return launch_pdl(gate_residual_stream_kernel<2>, grid, dim3(static_cast<unsigned>(nblocks / 2 * 32)), smem,
+                        stream, 1, a);
+    return launch_pdl(gate_residual_stream_kernel<1>, grid, dim3(static_cast<unsigned>(nblocks * 32)), smem, stream,
+                      1, a);
   }
   a.cluster = gate_cluster_size(a.dim);
   const unsigned threads = static_cast<unsigned>(a.dim / kBlockCh / a.cluster * 32);

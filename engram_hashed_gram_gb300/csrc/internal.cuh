@@ -164,7 +164,10 @@ struct GateArgs {
   float clamp;
   float inv_sqrt_dim;
   int32_t cluster;        // CTAs per token (set by launch_gate)
+  unsigned long long* err;  // device error word (bounded waits), or nullptr
+  int32_t num_sms;        // SMs of the device (0: unknown)
 };
+cudaError_t gate_prepare();   // per-device one-time kernel attributes
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t stream);
 
 // kv[m, n] = bf16(sum over splits, in order, of part[s, m, n])

@@ -218,16 +218,17 @@ def test_fused_epilogue_matches_split_path(tiny, B, T, mask_frac):
     fused.close()
 
 
-def test_wide_gate_kernel_matches_cluster_kernel(tiny):
-    """Batches of 256 tokens and more take the one-CTA-per-token gate kernel,
-    smaller ones the 4-CTA cluster kernel; both form the sums in the same order,
-    so the same tokens give the same bits either way."""
+def test_stream_gate_kernel_matches_cluster_kernel(tiny):
+    """Batches of 256 tokens and more take the persistent streaming gate
+    kernel (one CTA per SM, several tokens each), smaller ones the 4-CTA
+    cluster kernel; both form the sums in the same order, so the same tokens
+    give the same bits either way."""
     w, inp = _inputs(tiny, 2, 512, mask_frac=0.1, seed=4)
     ids, x, mask = _dev(inp)
     layer = tiny["layer"]
     kv = layer.lookup_project(ids)
-    g_wide = torch.empty((2, 512, 4), dtype=torch.float32, device="cuda")
-    out_wide = layer.gate_apply(kv, x, mask, gates=g_wide)                  # 1024 tokens
+    g_stream = torch.empty((2, 512, 4), dtype=torch.float32, device="cuda")
+    out_stream = layer.gate_apply(kv, x, mask, gates=g_stream)              # 1024 tokens
     outs, gs = [], []
     for b in range(2):
         for t0 in range(0, 512, 128):                                      # 128 tokens per call
@@ -237,10 +238,17 @@ def test_wide_gate_kernel_matches_cluster_kernel(tiny):
             gs.append(g)
     st, _ = layer.sync_status()
     assert st == 0
-    assert torch.equal(out_wide.view(torch.int16), torch.cat(outs, dim=1).reshape(2, 512, 4, -1).view(torch.int16))
-    assert torch.equal(g_wide.view(torch.int32), torch.cat(gs, dim=1).reshape(2, 512, 4).view(torch.int32))
-    summary = P.check_layer(w, inp, np.arange(1024), SD.device_bits(out_wide), g_wide.cpu().numpy(),
-                            SD.device_bits(kv), "wide gate 1024 tokens")
+    assert torch.equal(out_stream.view(torch.int16),
+                       torch.cat(outs, dim=1).reshape(2, 512, 4, -1).view(torch.int16))
+    assert torch.equal(g_stream.view(torch.int32), torch.cat(gs, dim=1).reshape(2, 512, 4).view(torch.int32))
+    # in place: out may be x
+    x2 = x.clone()
+    layer.gate_apply(kv, x2, mask, out=x2)
+    st, _ = layer.sync_status()
+    assert st == 0
+    assert torch.equal(x2.view(torch.int16), out_stream.view(torch.int16))
+    summary = P.check_layer(w, inp, np.arange(1024), SD.device_bits(out_stream), g_stream.cpu().numpy(),
+                            SD.device_bits(kv), "streaming gate 1024 tokens")
     print(summary)
 
 
