@@ -84,6 +84,7 @@ ENGRAM_FUNCS = {
     "engram_lookup": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p]),
     "engram_sync_status": (c_int32, [c_void_p, c_void_p, POINTER(c_int64)]),
     "engram_plan": (c_int32, [c_void_p, c_int64, POINTER(c_int32), POINTER(c_int32)]),
+    "engram_forward_kernels": (c_int32, [c_void_p, c_int64, POINTER(c_int32)]),
     "engram_set_sm_budget": (c_int32, [c_void_p, c_int32]),
     "engram_test_hook": (c_int32, [c_void_p, c_int32]),
     "engram_forward_noalloc": (c_int32, [POINTER(EngramConfig), POINTER(EngramWeights), c_void_p, c_void_p,

@@ -334,7 +334,7 @@ const char* engram_status_string(engram_status s) {
   return "unknown status";
 }
 
-int32_t engram_abi_version(void) { return 101; }
+int32_t engram_abi_version(void) { return 102; }
 
 engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w) {
   if (out == nullptr || cfg == nullptr || w == nullptr) return ENGRAM_EINVAL;
@@ -571,6 +571,21 @@ engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, int32_t* spli
   const Plan p = make_plan(ctx, m_tokens);
   if (splits != nullptr) *splits = p.splits;
   if (ctas != nullptr) *ctas = p.ctas;
+  return ENGRAM_OK;
+}
+
+engram_status engram_forward_kernels(const engram_ctx* ctx, int64_t m_tokens, int32_t* kernels) {
+  if (ctx == nullptr || m_tokens < 0 || kernels == nullptr) return ENGRAM_EINVAL;
+  if (m_tokens == 0) {
+    *kernels = 0;
+    return ENGRAM_OK;
+  }
+  const Plan p = make_plan(ctx, m_tokens);
+  if (ctx->cfg.fuse_gate && fuses(ctx, p, m_tokens)) {
+    *kernels = 2;                                   // gather, projection with the gate in its epilogue
+  } else {
+    *kernels = 3 + (p.rem_splits > 0 ? 1 : 0);      // gather, projection, [remainder sums], gate
+  }
   return ENGRAM_OK;
 }
 

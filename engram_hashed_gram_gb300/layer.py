@@ -172,6 +172,12 @@ class EngramLayer:
         check(self._lib.engram_plan(self._ctx, m_tokens, ctypes.byref(s), ctypes.byref(c)), "engram_plan")
         return s.value, c.value
 
+    def forward_kernels(self, m_tokens):
+        """How many kernels one forward over m_tokens tokens launches."""
+        k = ctypes.c_int32(0)
+        check(self._lib.engram_forward_kernels(self._ctx, m_tokens, ctypes.byref(k)), "engram_forward_kernels")
+        return k.value
+
     def set_sm_budget(self, sms: int):
         """At most `sms` SMs for the projection's grid (0 = all of them)."""
         check(self._lib.engram_set_sm_budget(self._ctx, sms), "engram_set_sm_budget")

@@ -196,11 +196,17 @@ ENGRAM_API engram_status engram_sync_status(engram_ctx* ctx, engram_stream_t str
 /* Split-K factor and CTA count the projection would use for B*T = m_tokens on
  * this context's device (for tests and benchmarks; queues nothing). */
 ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, int32_t* splits, int32_t* ctas);
-/* (Without split-K, when the tiles fill only part of a last wave of the grid,
- * the plan also cuts those last tiles into 2-4 K ranges whose fp32 sums are
- * added in order by the last range to finish; this changes kv's summation
- * order for those tiles, not its tolerance.  Contexts with max_tokens <= 128
- * or fuse_gate set keep whole tiles.) */
+/* (Without split-K, when a small number of tiles would fill only part of a
+ * last wave of the grid, the plan also cuts those last tiles into 2-4 K ranges
+ * whose fp32 sums a small kernel after the projection adds up in range order;
+ * this changes kv's summation order for those tiles, not its tolerance.
+ * Contexts with max_tokens <= 128 or fuse_gate set keep whole tiles.) */
+
+/* Number of kernels one engram_forward over m_tokens tokens launches on this
+ * context (gather, projection, the remainder sums when the plan has them, gate;
+ * 2 with the fused gate epilogue; 0 for no tokens).  Queues nothing.
+ * ENGRAM_EINVAL for a NULL context or pointer or a negative count. */
+ENGRAM_API engram_status engram_forward_kernels(const engram_ctx* ctx, int64_t m_tokens, int32_t* kernels);
 
 /* Caps the number of SMs the projection's persistent grid occupies (and that
  * its split-K plan is made for) at `sms`; 0 or more than the device has

@@ -93,7 +93,7 @@ int main(void) {
 
 def test_host_only_entry_points(libs):
     lib = libs.engram()
-    assert lib.engram_abi_version() == 101
+    assert lib.engram_abi_version() == 102
     for code, text in ((0, b"ok"), (-1, b"invalid argument"), (-4, b"hash id outside the table"),
                        (-5, b"kernel wait timed out"), (-6, b"unsupported shape or format"), (7, b"unknown status")):
         assert lib.engram_status_string(code) == text

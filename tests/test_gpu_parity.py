@@ -302,6 +302,10 @@ def test_remainder_split_tiles(tiny):
         split = layer.gate_apply(kv, x, mask, gates=gates)
         assert layer.sync_status()[0] == 0
         assert layer.plan(1300) == (1, 152)
+        # gather, projection, the remainder's sums, gate; no remainder at 1,216 tokens (8 full waves)
+        assert layer.forward_kernels(1300) == 4
+        assert layer.forward_kernels(1216) == 3
+        assert layer.forward_kernels(64) == 3 and layer.forward_kernels(0) == 0
         assert torch.equal(out.view(torch.int16), split.view(torch.int16))
         M = 1300
         tok = P.sample_tokens(M, 48, np.random.default_rng(8), must=[1279, 1280, 1299])
