@@ -134,9 +134,10 @@ GEMM_SOURCES = ["engram_hashed_gram_gb300/csrc/gemm.cu", "engram_hashed_gram_gb3
                 "engram_hashed_gram_gb300/csrc/internal.cuh"]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, plan=None):
     """DRAM bytes per launch of the projection kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+    summary, if it was taken on the current kernel source (and, when the record
+    names one, the same plan: split-K factor x CTAs); else None."""
     p = os.path.join(ROOT, "profiles", "wkv_gemm_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -144,6 +145,8 @@ def recorded_traffic(workload):
     for line in open(p):
         kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
         if kv.get("workload") == workload and kv.get("source_sha256") == digest:
+            if plan is not None and "plan" in kv and kv["plan"] != "%dx%d" % tuple(plan):
+                continue
             return float(kv["dram_bytes_per_launch"])
     return None
 
@@ -451,7 +454,7 @@ def run_ours(args, w, rank, world, local_rank):
             # the peak a dense GEMM holds for seconds under the power cap
             roof["frac_of_sustained"] = roof["achieved"] / pk["bf16_tflops_sustained"]
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(w.name)
+    roof["traffic"] = recorded_traffic(w.name, (splits, ctas))
     roof["kernel"] = "wkv_gemm_kernel (tcgen05 projection)"
     roof["peak_source"] = pk["source"]
     roof["algorithmic_bytes_per_launch"] = pbytes

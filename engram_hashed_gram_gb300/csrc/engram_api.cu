@@ -94,7 +94,14 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
   auto waves = [&](int64_t units) { return (units + sms - 1) / sms; };
   int32_t best = 1;
   int64_t best_cost = waves(tiles) * kbt;
-  if (M <= kSplitMaxTokens && M <= c->part_tokens) {
+  // A small batch streams the weight at the HBM rate once at least 5/8 of the
+  // SMs stream it (measured on GB300: 100 whole-K tiles on 100 of 152 SMs,
+  // decode 64 tokens 56.6 -> 54.6 us for the projection, against three K
+  // ranges on all 152 SMs), and without split-K the epilogue stores bf16 kv
+  // and the gate reads it instead of the fp32 partial sums.  Split-K is for
+  // fewer tiles than that, or more than one wave of them (an SM budget).
+  const bool streams_whole = tiles <= sms && tiles * 8 >= sms * 5;
+  if (M <= kSplitMaxTokens && M <= c->part_tokens && !streams_whole) {
     const int32_t cand[] = {2, 3, 4, 6, 8};
     for (int32_t s : cand) {
       if (s > kMaxSplits || kbt % s != 0) continue;

@@ -105,17 +105,25 @@ def _kv_report(err, bound):
             f"{cols[:8].tolist()}; by row quarter {by_rq.tolist()}, by column half {by_cq.tolist()}")
 
 
+@pytest.mark.parametrize("budget", [0, 64])
 @pytest.mark.parametrize("B,T", [(1, 16), (64, 1), (2, 100), (1, 300)])
-def test_fp8_projection_kv(mx, B, T):
+def test_fp8_projection_kv(mx, B, T, budget):
     """lookup_project with the MXFP8 weight against the oracle's
-    project_mxfp8, element by element (split-K plans for B*T <= 128, the
-    single-pass plan above, several M tiles and a ragged tail)."""
+    project_mxfp8, element by element (whole-K plans; split-K plans with the
+    projection capped at 64 SMs; several M tiles and a ragged tail)."""
     w, inp = _inputs(mx, B, T, bad_ids=2)
     ids, _, _ = _dev(inp)
     layer = mx["layer"]
-    kv = layer.lookup_project(ids)
-    st, _ = layer.sync_status()
+    layer.set_sm_budget(budget)
+    try:
+        kv = layer.lookup_project(ids)
+        plan = layer.plan(B * T)
+        st, _ = layer.sync_status()
+    finally:
+        layer.set_sm_budget(0)
     assert st == 0
+    if budget and B * T <= 128:
+        assert plan[0] > 1
     M = B * T
     e = P.oracle_rows(w, inp, np.arange(M))
     ref = O.project_mxfp8(e, inp.wkv, inp.wkv_scale)
@@ -123,7 +131,7 @@ def test_fp8_projection_kv(mx, B, T):
     bound = P.kv_bound(e, P.weight_values(inp), ref, w.K, splits=8)
     err = np.abs(got - O.bf16_value(ref))
     assert np.all(err <= bound), _kv_report(err, bound)
-    print(f"B={B} T={T} plan={layer.plan(M)} kv differing from the oracle: {float((err > 0).mean()):.4f}")
+    print(f"B={B} T={T} plan={plan} kv differing from the oracle: {float((err > 0).mean()):.4f}")
 
 
 @pytest.mark.parametrize("B,T,mask_frac", [(1, 16, 0.0), (64, 1, 0.2), (3, 70, 0.1), (200, 1, 0.0)])

@@ -1,8 +1,8 @@
 """GPU parity of the CUDA path against the oracle, through the C ABI, on the
 tiny table (24 prime ranges above 4096, 100,776 rows): shapes that span one
-and several 128-token tiles with ragged tails, the split-K decode plan and the
-single-pass prefill plan, masks, in-place calls, out-of-range ids and argument
-errors."""
+and several 128-token tiles with ragged tails, the whole-K decode plan, the
+split-K plan (under an SM budget) and the single-pass prefill plan, masks,
+in-place calls, out-of-range ids and argument errors."""
 import dataclasses
 
 import numpy as np
@@ -190,7 +190,7 @@ def test_empty_batch_is_a_no_op(tiny):
     assert layer.sync_status()[0] == 0
 
 
-@pytest.mark.parametrize("B,T,mask_frac", [(1, 150, 0.1), (300, 1, 0.0), (7, 100, 0.3)])
+@pytest.mark.parametrize("B,T,mask_frac", [(1, 150, 0.1), (300, 1, 0.0), (7, 100, 0.3), (64, 1, 0.2), (1, 16, 0.0)])
 def test_fused_epilogue_matches_split_path(tiny, B, T, mask_frac):
     """fuse_gate: the gate and residual add run in the projection's epilogue
     (plans without split-K); the result must equal lookup_project + gate_apply
@@ -282,6 +282,36 @@ def test_bounded_wait_runs_out_and_the_context_recovers(tiny):
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     finally:
         fused.close()
+
+
+@pytest.mark.parametrize("budget", [48, 96])
+def test_split_k_plans(tiny, budget):
+    """Decode batches on all SMs take whole-K tiles; with the projection capped
+    at fewer SMs than tiles the plan cuts K (fp32 partial sums, summed by the
+    gate kernel and by lookup_project's reduction).  Those plans against the
+    oracle, and forward against lookup_project + gate_apply bit for bit."""
+    layer = tiny["layer"]
+    assert layer.plan(64)[0] == 1
+    layer.set_sm_budget(budget)
+    try:
+        for B, T in [(64, 1), (1, 16), (3, 37)]:
+            M = B * T
+            splits, ctas = layer.plan(M)
+            assert splits > 1 and ctas <= budget
+            w, inp = _inputs(tiny, B, T, mask_frac=0.1, seed=9)
+            ids, x, mask = _dev(inp)
+            out = layer.forward(ids, x, mask)
+            kv = layer.lookup_project(ids)
+            gates = torch.empty((B, T, 4), dtype=torch.float32, device="cuda")
+            split = layer.gate_apply(kv, x, mask, gates=gates)
+            assert layer.sync_status()[0] == 0
+            assert torch.equal(out.view(torch.int16), split.view(torch.int16))
+            summary = P.check_layer(w, inp, np.arange(M), SD.device_bits(out), gates.cpu().numpy(),
+                                    SD.device_bits(kv), f"split-K {splits} B={B} T={T}")
+            print(f"budget {budget}: B={B} T={T} plan={(splits, ctas)} {summary}")
+    finally:
+        layer.set_sm_budget(0)
+    assert layer.plan(64)[0] == 1
 
 
 def test_remainder_split_tiles(tiny):
