@@ -117,7 +117,10 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   auto waves = [&](int64_t u) { return (u + sms - 1) / sms; };
   int32_t splits = 1;
   int64_t best = waves(tiles) * kbt;
-  for (int32_t sp = 2; sp <= kMaxSplits; ++sp) {
+  // whole-K tiles once they fill 5/8 of the grid in one wave (they stream the
+  // weight at the HBM rate), as engram_forward's plan does
+  const bool streams_whole = tiles <= sms && tiles * 8 >= static_cast<int64_t>(sms) * 5;
+  for (int32_t sp = 2; sp <= kMaxSplits && !streams_whole; ++sp) {
     if (kbt % sp != 0) continue;
     const int64_t cost = waves(tiles * sp) * (kbt / sp);
     if (cost < best) {
