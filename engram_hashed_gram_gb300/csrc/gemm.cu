@@ -5,9 +5,11 @@
 // accumulation.
 //
 // Design (sm_103a, one CTA per SM, persistent):
-//  * a work unit is a 128 x 256 output tile restricted to one K range
-//    (split-K, or the remainder split of a small last wave); units are dealt
-//    round-robin to the CTAs;
+//  * a work unit is a 128 x 256 output tile over the whole K (decode: the 100
+//    tiles on 100 CTAs already stream the weight at the HBM rate), or over
+//    one K range (split-K for fewer tiles or a capped SM budget, or the
+//    remainder split of a small last wave); units are dealt round-robin to
+//    the CTAs;
 //  * warp 0 (one thread) streams A = E[A_ROWS rows, 64 k] with a 2-D TMA copy
 //    (128-byte swizzle) and B = W[256 rows, 64 k] as one contiguous 32 KB bulk
 //    copy of the weight's tile-packed copy (packed at create time exactly as
@@ -20,6 +22,12 @@
 //    bf16 kv (round to nearest even) or the fp32 partial sums of a K range,
 //    through a per-warp shared-memory tile so that stores are row segments;
 //  * no cluster, no multicast: the L2 serves the reuse of E and W across CTAs.
+// FP8 (the MXFP8 weight): A and B are e4m3 codes, K = 128 per stage, the E8M0
+// scales ride with each stage and tcgen05.cp moves them into tensor memory
+// for tcgen05.mma kind::mxf8f6f4.block_scale (one accumulator: the scales use
+// the second one's columns).  BULK (bf16, 2,048 tokens and more): the
+// epilogue sends each lane's row segment with a bulk copy.  FUSED: the gate
+// and the residual add run in the epilogue (engram_config.fuse_gate).
 // Variants: A_ROWS = 128 with 4 stages in general; for batches of at most 64
 // or 32 tokens the A box holds only 64 or 32 rows, and the shared memory that
 // frees goes to a deeper ring (5 stages), i.e. more of the weight stream in
