@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(MAX_THREADS) gate_residual_kernel(const GateAr
   // x and the mask are inputs of the call, written before the gather ran, so
   // they may be read before the projection has finished
   if (a.mask != nullptr && a.mask[m] == 0) {
-    // "pass through untouched": the streams are copied, the gate is 0
+    // a masked token leaves the streams as they were: copied, gate 0
     grid_dependency_wait();
     if (om != xm) {
       for (int s = 0; s < HC; ++s)
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kMaxBlocks / BPW * 32, 1) gate_residual_stream
     uint16_t* om = a.out + m * HC * D;
 
     if (a.mask != nullptr && a.mask[m] == 0) {
-      // "pass through untouched": the streams are copied, the gate is 0
+      // a masked token leaves the streams as they were: copied, gate 0
 #pragma unroll
       for (int j = 0; j < BPW; ++j)
         for (int s = 0; s < HC; ++s)

@@ -17,7 +17,7 @@
  *      gate = sigmoid(copysign(sqrt(max(|dot|, clamp)), dot)), 0 where the
  *      token mask is False;
  *   6. out = bf16(h + gate * value) for every stream; a masked token's streams
- *      are returned bit-for-bit ("pass through untouched").
+ *      are returned bit-for-bit (the excerpt's docstring leaves them as they are).
  * The split into lookup+projection and gating follows zhuai.tech "Engram in
  * DeepSeek V4.1 Flash" (section "Run projection early: overlap CPU work with
  * the GPU"): the lookup and projection depend only on the ids and may run

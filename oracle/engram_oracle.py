@@ -24,7 +24,7 @@ written out below from its definition.
 Readings where the pages leave a step open (each is also listed in the design
 notes of the repository):
   * masked tokens (``token_mask`` False) return the input bits unchanged: the
-    excerpt's docstring says such positions "pass through untouched"; a literal
+    excerpt's docstring says such positions are left as they are; a literal
     ``h + 0*value`` would differ only for h = -0.0 or a non-finite value.
   * ids outside [0, R) give a zero row, as the single-rank case of the sharded
     embedding does (its out-of-shard mask zeroes the row).
