@@ -280,6 +280,52 @@ __device__ __forceinline__ void plain_epilogue(const GemmArgs& a, uint32_t t_row
   if constexpr (bulk) bulk_wait_all();               // the unit's rows are in global memory
 }
 
+// bf16 kv of the warp's 32 rows for the FP8 kernel, whose single accumulator
+// keeps the next tile's MMAs waiting for the epilogue: the lane's whole row
+// (256 columns, as 128 bf16 pairs in registers) leaves tensor memory first,
+// the accumulator is released (tempty_bar), and only then does the row go out
+// through the warp's shared-memory tile, as in plain_epilogue's bf16 path and
+// with the same values.
+__device__ __forceinline__ void bf16_epilogue_release_first(const GemmArgs& a, uint32_t t_row, int64_t m0, int nt,
+                                                            int lane, uint32_t stage, uint64_t* tempty_bar) {
+  const bool any = m0 < a.M;                         // some row of this quarter is a token
+  uint32_t packed[kBN / 32][16];
+  if (any) {
+#pragma unroll
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * 32), r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) packed[c][j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty_bar);
+  if (!any) return;
+  const uint32_t mine = stage + static_cast<uint32_t>(lane * kPlainPitch);
+#pragma unroll
+  for (int c = 0; c < kBN / 32; ++c) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_shared_v4(mine + 16 * j,
+                   make_uint4(packed[c][4 * j], packed[c][4 * j + 1], packed[c][4 * j + 2], packed[c][4 * j + 3]));
+    __syncwarp();
+    const int n0 = nt * kBN + c * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = i * 8 + (lane >> 2);
+      const int q = lane & 3;
+      if (m0 + row < a.M) {
+        const uint4 v = ld_shared_v4(stage + static_cast<uint32_t>(row * kPlainPitch + q * 16));
+        *reinterpret_cast<uint4*>(a.kv + (m0 + row) * a.N + n0 + q * 8) = v;
+      }
+    }
+    __syncwarp();                                    // the tile is rewritten by the next chunk
+  }
+}
+
 // ---------------------------------------------------------------- fused epilogue
 // The fused epilogue forms the gate kernel's sums in the gate kernel's order
 // (gate.cu): a 256-channel block of one stream is 32 groups of 8 channels; a
@@ -705,8 +751,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      bool released = false;                         // the accumulator already handed back
       if constexpr (!FUSED) {
-        if (remainder_unit(a, u)) {
+        if (FP8 && a.out_mode == kOutBf16 && !remainder_unit(a, u)) {
+          bf16_epilogue_release_first(a, t_row, m - lane, nt, lane, smem_u32(epi), &tempty[acc]);
+          released = true;
+        } else if (remainder_unit(a, u)) {
           // remainder unit j (tile j / rem_splits, K range sp): its fp32 sums go to
           // the workspace; launch_reduce_remainder adds the ranges up afterwards
           const int64_t j = u - a.full_units;
@@ -722,9 +772,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ok = false;
         break;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      }
       if (++acc == kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
