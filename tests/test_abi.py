@@ -139,3 +139,14 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_binding_refuses_a_host_table_the_device_cannot_read():
+    """EngramLayer takes a CUDA table or a pinned host table; an ordinary
+    (pageable) host tensor is refused before anything reaches the library."""
+    import torch
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    table = torch.zeros((4, 256), dtype=torch.uint8)
+    assert not table.is_pinned()
+    with pytest.raises(ValueError, match="pinned"):
+        EngramLayer(table, torch.zeros((4, 2)), torch.zeros(1), torch.zeros(1), torch.zeros(1))
