@@ -29,7 +29,6 @@ import argparse
 import dataclasses
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
