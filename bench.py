@@ -6,11 +6,12 @@
 
 A step is one engram_forward (gather + dequantise -> tcgen05 wkv projection ->
 gate + residual add) over one batch of synthetic inputs resident in HBM.  The
-default workload is the decode batch (B=64, T=1, 24 prime row ranges above
-2^20: 25,169,534 rows, 6.4 GB of fp8 codes), the configuration the layer's
-tokens/s metric is quoted on; the other workloads (tiny, Zipf prefill, skewed
-decode, full-size table) are selectable with --workload and are parity-test
-cases.
+default workload is the largest configuration of the layer's benchmark that
+one GPU holds: the full-size table (384,016,682 rows, 98.3 GB of fp8 codes plus
+3.1 GB of scales) with a prefill batch of B=2, T=8192.  The same JSON line
+carries a `per_config` list with the benchmark's other configurations (tiny,
+decode batch, Zipf prefill, skewed large decode), each measured the same way
+(`--no-per-config` leaves them out; `--workload` picks another main one).
 
 One JSON line is printed by rank 0 (see the keys below).  `value` is tokens/s
 over all ranks, timed on the device with CUDA events around each step; the L2
@@ -41,7 +42,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Engram layer tokens/s (prefill, decode); gather HBM GB/s; % of roofline"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "decode_64x1"
+DEFAULT_WORKLOAD = "full_2x8192"
+# the benchmark's other configurations, measured after the main one and reported in `per_config`
+PER_CONFIG = ["tiny_1x16", "decode_64x1", "prefill_1x4096_zipf", "decode_512x1_skew"]
+PER_CONFIG_CPU_SECONDS = 4.0
 ARGS = None
 FLUSH_BYTES = 256 << 20
 
@@ -514,6 +518,15 @@ def run_ours(args, w, rank, world, local_rank):
     return result
 
 
+def per_config_entry(r):
+    """The keys of one configuration's measurement that the per_config list carries."""
+    keys = ("value", "unit", "ms_per_step", "step_ms_spread", "dtype", "e2e", "gpu_launches", "roofline",
+            "layer_roofline", "stages_ms", "gather_gbs", "plan", "clocks", "cpu_baseline")
+    out = {"workload": r["config"]["workload"], "config": r["config"]}
+    out.update({k: r[k] for k in keys if k in r})
+    return out
+
+
 def aggregate_over_ranks(total_ms, e2e_ms, tokens_per_rank, steps, world, device):
     """Whole-job throughput of a weak-scaling run: every rank processed
     tokens_per_rank tokens per step, and the job took as long as its slowest
@@ -719,6 +732,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the main workload only (no per_config list)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--component", choices=["layer", "hash", "runahead"], default="layer",
                     help="hash: time the n-gram hash (engram_hash) alone; runahead: two Engram layers run "
@@ -771,6 +786,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     res = run_ours(args, w, rank, world, local_rank)
+    if not args.no_per_config and args.workload == DEFAULT_WORKLOAD and args.prime_base is None:
+        sub = argparse.Namespace(**dict(vars(args), cpu_seconds=min(args.cpu_seconds, PER_CONFIG_CPU_SECONDS)))
+        res["per_config"] = [per_config_entry(run_ours(sub, synth.workload(name), rank, world, local_rank))
+                             for name in PER_CONFIG]
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

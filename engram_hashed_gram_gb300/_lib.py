@@ -46,6 +46,7 @@ class EngramConfig(ctypes.Structure):
         ("check_ids", c_int32),
         ("fuse_gate", c_int32),
         ("wkv_fmt", c_int32),
+        ("row_offset", c_int64),
     ]
 
 
@@ -82,6 +83,7 @@ ENGRAM_FUNCS = {
     "engram_gate_apply": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64,
                                     c_void_p]),
     "engram_lookup": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p]),
+    "engram_forward_rows": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_void_p]),
     "engram_sync_status": (c_int32, [c_void_p, c_void_p, POINTER(c_int64)]),
     "engram_plan": (c_int32, [c_void_p, c_int64, POINTER(c_int32), POINTER(c_int32)]),
     "engram_forward_kernels": (c_int32, [c_void_p, c_int64, POINTER(c_int32)]),

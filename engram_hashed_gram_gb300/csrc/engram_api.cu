@@ -54,22 +54,6 @@ constexpr int64_t kSplitMaxTokens = 128;   // split-K only while one M tile cove
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Whether kernels on `device` can read p at address p: memory of that device,
-// managed memory, or pinned host memory mapped at the same address.
-bool device_readable(const void* p, int device) {
-  cudaPointerAttributes at{};
-  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  switch (at.type) {
-    case cudaMemoryTypeDevice: return at.device == device;
-    case cudaMemoryTypeManaged: return true;
-    case cudaMemoryTypeHost: return at.devicePointer == p;
-    default: return false;
-  }
-}
-
 struct Plan {
   int32_t splits;
   int32_t ctas;
@@ -182,6 +166,7 @@ GatherArgs gather_args(const engram_ctx* c, const int64_t* ids, uint16_t* out, i
   g.out = out;
   g.rows_total = M * c->cfg.n_cols;
   g.R = c->cfg.num_rows;
+  g.row0 = c->cfg.row_offset;
   g.head_dim = c->cfg.head_dim;
   g.scale_block = c->cfg.scale_block;
   g.scale_fmt = c->cfg.scale_fmt;
@@ -200,11 +185,13 @@ struct FusedIO {
 
 bool fuses(const engram_ctx* c, const Plan& p, int64_t M) { return !c->fp8 && p.splits == 1 && gemm_can_fuse(M); }
 
-// gathered rows -> projection.  With `fused` and a fusable plan it writes the
-// layer's output; otherwise bf16 kv to kv_out when splits == 1 and the fp32
-// partial sums to the context when splits > 1.
-engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint16_t* kv_out, const FusedIO* fused,
-                             Plan* plan_out, cudaStream_t stream) {
+// gathered rows -> projection.  The rows are gathered from `ids` into the
+// context's buffer, or, with rows_in (bf16 weight only), taken from the
+// caller.  With `fused` and a fusable plan it writes the layer's output;
+// otherwise bf16 kv to kv_out when splits == 1 and the fp32 partial sums to
+// the context when splits > 1.
+engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* rows_in, int64_t M, uint16_t* kv_out,
+                             const FusedIO* fused, Plan* plan_out, cudaStream_t stream) {
   if (cudaSetDevice(c->device) != cudaSuccess) return ENGRAM_ECUDA;
   const Plan p = make_plan(c, M);
   const bool fuse = fused != nullptr && c->cfg.fuse_gate && fuses(c, p, M);
@@ -215,7 +202,12 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
     g.n_zero = p.m_tiles * 8;
   }
   mark(c, 0, stream);
-  if (c->fp8) {
+  if (rows_in != nullptr) {
+    // no gather: clear what it would have cleared for the fused epilogue
+    if (fuse && cudaMemsetAsync(c->counters, 0, static_cast<size_t>(p.m_tiles) * 8 * sizeof(uint32_t), stream) !=
+                    cudaSuccess)
+      return ENGRAM_ECUDA;
+  } else if (c->fp8) {
     if (launch_gather_codes(g, c->cfg.n_cols, c->codes, c->sfa, c->num_sms, stream) != cudaSuccess)
       return ENGRAM_ECUDA;
   } else if (launch_gather(g, c->num_sms, stream) != cudaSuccess) {
@@ -278,7 +270,9 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, int64_t M, uint1
     a.clamp = c->cfg.clamp;
     a.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c->cfg.dim)));
   }
-  const void* rows = c->fp8 ? static_cast<const void*>(c->codes) : static_cast<const void*>(c->rows);
+  const void* rows = rows_in != nullptr ? static_cast<const void*>(rows_in)
+                     : c->fp8        ? static_cast<const void*>(c->codes)
+                                     : static_cast<const void*>(c->rows);
   if (launch_gemm(rows, c->tmW, a, p.ctas, stream) != cudaSuccess) return ENGRAM_ECUDA;
   if (rem && launch_reduce_remainder(a, c->num_sms, stream) != cudaSuccess) return ENGRAM_ECUDA;
   mark(c, 2, stream);
@@ -324,6 +318,30 @@ void free_ctx(engram_ctx* c) {
   delete c;
 }
 
+// The layer from ids (gathered here) or from caller rows: projection, then the
+// gate in the projection's epilogue or in the gate kernel.
+engram_status forward_from(engram_ctx* ctx, const int64_t* hash_ids, const uint16_t* rows, const uint16_t* x,
+                           const uint8_t* token_mask, uint16_t* out, int64_t M, cudaStream_t s) {
+  Plan p{};
+  const FusedIO io{x, token_mask, out};
+  engram_status st = run_projection(ctx, hash_ids, rows, M, ctx->kv, &io, &p, s);
+  if (st != ENGRAM_OK) return st;
+  if (ctx->cfg.fuse_gate && fuses(ctx, p, M)) {   // the projection's epilogue applied the gate
+    mark(ctx, 3, s);
+    return ENGRAM_OK;
+  }
+  GateArgs g = gate_args(ctx, x, token_mask, out, nullptr, M);
+  if (p.splits == 1) {
+    g.kv = ctx->kv;
+  } else {
+    g.part = ctx->part;
+    g.splits = p.splits;
+  }
+  st = cuda_status(launch_gate(g, s));
+  mark(ctx, 3, s);
+  return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -341,14 +359,15 @@ const char* engram_status_string(engram_status s) {
   return "unknown status";
 }
 
-int32_t engram_abi_version(void) { return 102; }
+int32_t engram_abi_version(void) { return 103; }
 
 engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w) {
   if (out == nullptr || cfg == nullptr || w == nullptr) return ENGRAM_EINVAL;
   *out = nullptr;
   const engram_config& c = *cfg;
   if (c.dim <= 0 || c.hc_mult <= 0 || c.n_cols <= 0 || c.head_dim <= 0 || c.scale_block <= 0 ||
-      c.num_rows < 0 || c.max_tokens < 0 || !(c.eps >= 0.0f) || !(c.clamp >= 0.0f))
+      c.num_rows < 0 || c.max_tokens < 0 || !(c.eps >= 0.0f) || !(c.clamp >= 0.0f) || c.row_offset < 0 ||
+      c.row_offset > INT64_MAX - c.num_rows)
     return ENGRAM_EINVAL;
   if (w->table == nullptr || w->scale == nullptr || w->wkv == nullptr || w->q_weight == nullptr ||
       w->k_weight == nullptr)
@@ -383,7 +402,9 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
     delete ctx;
     return ENGRAM_ECUDA;
   }
-  if (!device_readable(w->table, ctx->device) || !device_readable(w->scale, ctx->device)) {
+  if (!device_readable(w->table, ctx->device) || !device_readable(w->scale, ctx->device) ||
+      !device_readable(w->wkv, ctx->device) || !device_readable(w->q_weight, ctx->device) ||
+      !device_readable(w->k_weight, ctx->device) || (fp8 && !device_readable(w->wkv_scale, ctx->device))) {
     delete ctx;
     return ENGRAM_EINVAL;
   }
@@ -458,25 +479,21 @@ engram_status engram_forward(engram_ctx* ctx, const int64_t* hash_ids, const uin
   if (M == 0) return ENGRAM_OK;
   if (hash_ids == nullptr || x == nullptr || out == nullptr) return ENGRAM_EINVAL;
   if (!aligned(hash_ids, 8) || !aligned(x, 16) || !aligned(out, 16)) return ENGRAM_EINVAL;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  Plan p{};
-  const FusedIO io{x, token_mask, out};
-  st = run_projection(ctx, hash_ids, M, ctx->kv, &io, &p, s);
+  return forward_from(ctx, hash_ids, nullptr, x, token_mask, out, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+engram_status engram_forward_rows(engram_ctx* ctx, const uint16_t* rows, const uint16_t* x,
+                                  const uint8_t* token_mask, uint16_t* out, int64_t B, int64_t T,
+                                  engram_stream_t stream) {
+  if (ctx == nullptr) return ENGRAM_EINVAL;
+  if (ctx->fp8) return ENGRAM_EUNSUPPORTED;   // the MXFP8 projection reads the table's codes, not bf16 rows
+  int64_t M;
+  engram_status st = check_tokens(ctx, B, T, &M);
   if (st != ENGRAM_OK) return st;
-  if (ctx->cfg.fuse_gate && fuses(ctx, p, M)) {   // the projection's epilogue applied the gate
-    mark(ctx, 3, s);
-    return ENGRAM_OK;
-  }
-  GateArgs g = gate_args(ctx, x, token_mask, out, nullptr, M);
-  if (p.splits == 1) {
-    g.kv = ctx->kv;
-  } else {
-    g.part = ctx->part;
-    g.splits = p.splits;
-  }
-  st = cuda_status(launch_gate(g, s));
-  mark(ctx, 3, s);
-  return st;
+  if (M == 0) return ENGRAM_OK;
+  if (rows == nullptr || x == nullptr || out == nullptr) return ENGRAM_EINVAL;
+  if (!aligned(rows, 16) || !aligned(x, 16) || !aligned(out, 16)) return ENGRAM_EINVAL;
+  return forward_from(ctx, nullptr, rows, x, token_mask, out, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
 engram_status engram_lookup_project(engram_ctx* ctx, const int64_t* hash_ids, uint16_t* kv, int64_t B,
@@ -489,7 +506,7 @@ engram_status engram_lookup_project(engram_ctx* ctx, const int64_t* hash_ids, ui
   if (hash_ids == nullptr || kv == nullptr || !aligned(hash_ids, 8) || !aligned(kv, 16)) return ENGRAM_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Plan p{};
-  st = run_projection(ctx, hash_ids, M, kv, nullptr, &p, s);
+  st = run_projection(ctx, hash_ids, nullptr, M, kv, nullptr, &p, s);
   if (st != ENGRAM_OK) return st;
   if (p.splits > 1) st = cuda_status(launch_reduce_partials(ctx->part, p.splits, M, ctx->N, kv, ctx->num_sms, s));
   mark(ctx, 3, s);

@@ -88,6 +88,19 @@ __device__ __forceinline__ void load_partials(const float* part, int HC, int D, 
     for (int j = 0; j < 8; ++j) f[g][j] = round_bf16(f[g][j]);
 }
 
+// The thread's 8 channels of q_weight*k_weight for every stream.
+__device__ __forceinline__ void load_wprod(const float* wprod, int HC, int D, int d0, float (&w)[kMaxHc][8]) {
+#pragma unroll
+  for (int s = 0; s < kMaxHc; ++s) {
+    if (s < HC) {
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(wprod + s * D + d0));
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(wprod + s * D + d0) + 1);
+      w[s][0] = w0.x; w[s][1] = w0.y; w[s][2] = w0.z; w[s][3] = w0.w;
+      w[s][4] = w1.x; w[s][5] = w1.y; w[s][6] = w1.z; w[s][7] = w1.w;
+    }
+  }
+}
+
 // MAX_THREADS bounds the block: 160 for dim = 5120 in clusters of 4 (the
 // registers then hold a thread's x, weights and kv at once), kGateMaxThreads
 // for other shapes.
@@ -124,22 +137,20 @@ __global__ void __launch_bounds__(MAX_THREADS) gate_residual_kernel(const GateAr
     return;
   }
 
-  // the product q_weight * k_weight is formed at create time: it is read
-  // before the wait too
+  // The product q_weight * k_weight is formed when a context is created, long
+  // before this kernel, so it is read before the wait too -- unless the caller
+  // forms it in the same call (wprod_after_wait: the allocation-free entry
+  // point), where it is read after the wait like every other output of an
+  // earlier kernel.
   float h[kMaxHc][8], w[kMaxHc][8];
 #pragma unroll
-  for (int s = 0; s < kMaxHc; ++s) {
-    if (s < HC) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(xm + s * D + d0)), h[s]);
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0) + 1);
-      w[s][0] = w0.x; w[s][1] = w0.y; w[s][2] = w0.z; w[s][3] = w0.w;
-      w[s][4] = w1.x; w[s][5] = w1.y; w[s][6] = w1.z; w[s][7] = w1.w;
-    }
-  }
+  for (int s = 0; s < kMaxHc; ++s)
+    if (s < HC) unpack8(__ldg(reinterpret_cast<const uint4*>(xm + s * D + d0)), h[s]);
+  if (!a.wprod_after_wait) load_wprod(a.wprod, HC, D, d0, w);
 
   grid_dependency_wait();        // kv / the partial sums come from the projection
   grid_launch_dependents();
+  if (a.wprod_after_wait) load_wprod(a.wprod, HC, D, d0, w);
 
   float kv[kMaxHc + 1][8];       // the streams' keys, then the value
   if (FROM_PARTIALS) {
@@ -260,21 +271,21 @@ __global__ void __launch_bounds__(kMaxBlocks / BPW * 32, 1) gate_residual_stream
     fence_mbarrier_init();
     abort_flag = 0;
   }
-  // q_weight * k_weight, formed at create time, once per CTA
+  // q_weight * k_weight, once per CTA: before the wait when a context formed
+  // it at create time, after it when the caller formed it in the same call
+  // (wprod_after_wait)
   float w[BPW][kMaxHc][8];
+  if (!a.wprod_after_wait) {
 #pragma unroll
-  for (int j = 0; j < BPW; ++j)
-#pragma unroll
-    for (int s = 0; s < kMaxHc; ++s)
-      if (s < HC) {
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0[j]));
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wprod + s * D + d0[j]) + 1);
-        w[j][s][0] = w0.x; w[j][s][1] = w0.y; w[j][s][2] = w0.z; w[j][s][3] = w0.w;
-        w[j][s][4] = w1.x; w[j][s][5] = w1.y; w[j][s][6] = w1.z; w[j][s][7] = w1.w;
-      }
+    for (int j = 0; j < BPW; ++j) load_wprod(a.wprod, HC, D, d0[j], w[j]);
+  }
   __syncthreads();
   grid_dependency_wait();        // kv comes from the projection
   grid_launch_dependents();
+  if (a.wprod_after_wait) {
+#pragma unroll
+    for (int j = 0; j < BPW; ++j) load_wprod(a.wprod, HC, D, d0[j], w[j]);
+  }
 
   const uint64_t pol = policy_evict_first();
   const int64_t step = gridDim.x;

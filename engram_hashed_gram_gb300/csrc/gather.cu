@@ -1,8 +1,12 @@
 // Steps a1-a3 of the Engram layer: id range check, row gather and
 // dequantisation (atlas.klimoza.dev "deepseek-v4.1 / engram-second",
-// `ParallelEngramEmbedding.forward`): for row r = ids[i],
+// `ParallelEngramEmbedding.forward`): for row r = ids[i] - row0 (row0: the
+// global id of the table's first row, non-zero for one shard of a row-split
+// table),
 //   out[i, f] = bf16_rn( fp32(e4m3 code[r, f]) *_rn scale[r, f / scale_block] )
-// and a zero row when r is outside [0, R).
+// and a zero row when r is outside [0, R).  The difference is taken in
+// unsigned 64-bit arithmetic, so every id below row0 (however negative) wraps
+// past R and is outside too.
 //
 // One thread owns one 16-byte chunk of a row (16 codes): consecutive threads
 // read consecutive chunks of the same 256-byte row, so each row is one fully
@@ -57,9 +61,10 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int64_t row = i / cpr;
     const int ch = static_cast<int>(i - row * cpr);
-    const int64_t r = __ldg(a.ids + row);
+    const uint64_t ur = static_cast<uint64_t>(__ldg(a.ids + row)) - static_cast<uint64_t>(a.row0);
+    const int64_t r = static_cast<int64_t>(ur);
     uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
-    if (r >= 0 && r < a.R) {
+    if (ur < static_cast<uint64_t>(a.R)) {
       const uint4 c = ld_stream_v4(a.table + r * a.head_dim + ch * 16);
       const int blk = (ch * 16) / a.scale_block;
       float s;
@@ -101,8 +106,9 @@ __global__ void __launch_bounds__(256) gather_codes_kernel(GatherArgs a, int n_c
     const int ch = static_cast<int>(i - row * cpr);
     const int64_t m = row / n_cols;
     const int c = static_cast<int>(row - m * n_cols);
-    const int64_t r = __ldg(a.ids + row);
-    const bool valid = r >= 0 && r < a.R;
+    const uint64_t ur = static_cast<uint64_t>(__ldg(a.ids + row)) - static_cast<uint64_t>(a.row0);
+    const int64_t r = static_cast<int64_t>(ur);
+    const bool valid = ur < static_cast<uint64_t>(a.R);
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (valid) {
       v = ld_stream_v4(a.table + r * a.head_dim + ch * 16);

@@ -39,6 +39,25 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Whether kernels on `device` can read p at address p: memory of that device,
+// managed memory, or pinned host memory mapped at the same address.  Host code
+// only; it allocates nothing and queues nothing.  A pointer that fails it
+// (pageable host memory, another device's memory) would make the first kernel
+// that dereferences it fault.
+inline bool device_readable(const void* p, int device) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: return at.device == device;
+    case cudaMemoryTypeManaged: return true;
+    case cudaMemoryTypeHost: return at.devicePointer == p;
+    default: return false;
+  }
+}
+
 // ---- rows: gather + dequantise (steps a1-a3) ------------------------------
 struct GatherArgs {
   const int64_t* ids;       // [rows_total] global row ids (rows_total = M * n_cols)
@@ -46,7 +65,8 @@ struct GatherArgs {
   const void* scale;        // [R, head_dim/scale_block] fp32 or e8m0
   uint16_t* out;            // [rows_total, head_dim] bf16
   int64_t rows_total;
-  int64_t R;
+  int64_t R;                // rows of the table (of the shard)
+  int64_t row0;             // global id of its first row: id i reads row i - row0
   int32_t head_dim;
   int32_t scale_block;
   int32_t scale_fmt;
@@ -166,6 +186,8 @@ struct GateArgs {
   int32_t cluster;        // CTAs per token (set by launch_gate)
   unsigned long long* err;  // device error word (bounded waits), or nullptr
   int32_t num_sms;        // SMs of the device (0: unknown)
+  int32_t wprod_after_wait;  // wprod is written by a kernel of the same call: read it after the
+                             // dependency wait (otherwise it is read before, to hide its latency)
 };
 cudaError_t gate_prepare();   // per-device one-time kernel attributes
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t stream);

@@ -29,7 +29,7 @@ constexpr int64_t kMaxTokens = ENGRAM_NOALLOC_MAX_TOKENS;
 constexpr int64_t kMaxK = 6144;           // n_cols * head_dim
 constexpr int64_t kMaxN = 25600;          // dim * (hc_mult + 1)
 constexpr int64_t kMaxHcDim = 4 * 5120;   // hc_mult * dim
-constexpr int32_t kMaxSplits = 3;
+constexpr int32_t kMaxSplits = 3;            // sizes the partial sums at the V4.1 shape
 
 constexpr size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 constexpr size_t kErrBytes = 256;
@@ -44,20 +44,58 @@ static_assert(kScratchBytes == ENGRAM_NOALLOC_SCRATCH_BYTES, "header and impleme
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-unsigned char* g_dev_scratch[kMaxDevices] = {};
 
-// Device address of g_scratch on device `dev` (which must be current), looked
-// up once per device: the first call on a device does this set-up.
+// The driver's id of the context current on this thread (0 if none, or if the
+// driver entry points are unavailable).  Ids are never reused within a
+// process, unlike context handles.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+struct ScratchSlot {
+  unsigned long long context_id;   // the context the address belongs to
+  unsigned char* address;
+};
+std::mutex g_mu;
+ScratchSlot g_slots[kMaxDevices] = {};
+
+// Device address of g_scratch on device `dev` (which must be current).  The
+// address is looked up (cudaGetSymbolAddress, which also loads this module on
+// the device) at the first call on a device and again whenever the device's
+// context has changed since (after cudaDeviceReset the module, and with it the
+// array, lives at a new address); otherwise the cached address is used.
 cudaError_t scratch_address(int dev, unsigned char** out) {
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_dev_scratch[dev] == nullptr) {
+  ScratchSlot& slot = g_slots[dev];
+  const unsigned long long id = current_context_id();
+  if (slot.address == nullptr || id == 0 || slot.context_id != id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return e;
-    g_dev_scratch[dev] = static_cast<unsigned char*>(p);
+    slot.address = static_cast<unsigned char*>(p);
+    slot.context_id = current_context_id();   // the lookup made the device's context current
   }
-  *out = g_dev_scratch[dev];
+  *out = slot.address;
   return cudaSuccess;
 }
 
@@ -75,7 +113,7 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   const int64_t M = B * T;
   if (M > kMaxTokens) return ENGRAM_EINVAL;   // the static scratch holds ENGRAM_NOALLOC_MAX_TOKENS tokens
   if (c.dim <= 0 || c.hc_mult <= 0 || c.n_cols <= 0 || c.head_dim <= 0 || c.scale_block <= 0 || c.num_rows < 0 ||
-      !(c.eps >= 0.0f) || !(c.clamp >= 0.0f))
+      !(c.eps >= 0.0f) || !(c.clamp >= 0.0f) || c.row_offset < 0 || c.row_offset > INT64_MAX - c.num_rows)
     return ENGRAM_EINVAL;
   if (c.scale_fmt != ENGRAM_SCALE_F32 && c.scale_fmt != ENGRAM_SCALE_E8M0) return ENGRAM_EUNSUPPORTED;
   if (c.wkv_fmt != ENGRAM_WKV_BF16) return ENGRAM_EUNSUPPORTED;   // the MXFP8 weight needs a context's packed copy
@@ -101,6 +139,12 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return ENGRAM_ECUDA;
   if (major != 10 || minor != 3) return ENGRAM_EUNSUPPORTED;
+  // Every buffer the kernels will dereference must be readable by this device
+  // where it is: a pageable host pointer or another device's memory would make
+  // the first kernel that touches it fault.  Nothing is queued before this.
+  if (!device_readable(w->table, dev) || !device_readable(w->scale, dev) || !device_readable(w->wkv, dev) ||
+      !device_readable(w->q_weight, dev) || !device_readable(w->k_weight, dev))
+    return ENGRAM_EINVAL;
   unsigned char* base = nullptr;
   if (scratch_address(dev, &base) != cudaSuccess) return ENGRAM_ECUDA;
   auto* err = reinterpret_cast<unsigned long long*>(base);
@@ -109,7 +153,10 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   auto* part = reinterpret_cast<float*>(base + kErrBytes + kWprodBytes + kRowsBytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  // the split-K factor: engram_forward's rule, restricted to <= kMaxSplits
+  // the split-K factor: engram_forward's rule (whole-K tiles once they fill
+  // 5/8 of the grid in one wave, since they stream the weight at the HBM rate;
+  // otherwise the factor in {2, 3, 4, 6, 8} that minimises waves x K blocks),
+  // among the factors whose fp32 partial sums fit the scratch
   const int32_t m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
   const int32_t n_tiles = static_cast<int32_t>(N / kBN);
   const int32_t kbt = static_cast<int32_t>(K / kBK);
@@ -117,11 +164,11 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   auto waves = [&](int64_t u) { return (u + sms - 1) / sms; };
   int32_t splits = 1;
   int64_t best = waves(tiles) * kbt;
-  // whole-K tiles once they fill 5/8 of the grid in one wave (they stream the
-  // weight at the HBM rate), as engram_forward's plan does
   const bool streams_whole = tiles <= sms && tiles * 8 >= static_cast<int64_t>(sms) * 5;
-  for (int32_t sp = 2; sp <= kMaxSplits && !streams_whole; ++sp) {
-    if (kbt % sp != 0) continue;
+  const int32_t cand[] = {2, 3, 4, 6, 8};
+  for (int32_t sp : cand) {
+    if (streams_whole || kbt % sp != 0) continue;
+    if (static_cast<size_t>(sp) * M * N * sizeof(float) > kPartBytes) continue;
     const int64_t cost = waves(tiles * sp) * (kbt / sp);
     if (cost < best) {
       best = cost;
@@ -132,6 +179,11 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   // the error word is the only scratch that must start at zero; the rest is
   // overwritten before it is read
   if (cudaMemsetAsync(err, 0, 2 * sizeof(unsigned long long), s) != cudaSuccess) return ENGRAM_ECUDA;
+  // q_weight*k_weight is formed on every call, into the scratch.  Ordering: the
+  // gather waits (griddepcontrol.wait) for this kernel; the projection waits
+  // for the gather; the gate kernel reads the product only after its own wait
+  // (wprod_after_wait below), so no kernel of this call reads it early, and the
+  // previous call's product left in the array is never read.
   if (launch_weight_product(w->q_weight, w->k_weight, wprod, static_cast<int64_t>(c.hc_mult) * c.dim, s) !=
       cudaSuccess)
     return ENGRAM_ECUDA;
@@ -143,6 +195,7 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   g.out = rows;
   g.rows_total = M * c.n_cols;
   g.R = c.num_rows;
+  g.row0 = c.row_offset;
   g.head_dim = c.head_dim;
   g.scale_block = c.scale_block;
   g.scale_fmt = c.scale_fmt;
@@ -182,6 +235,7 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   ga.eps = c.eps;
   ga.clamp = c.clamp;
   ga.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.dim)));
+  ga.wprod_after_wait = 1;                    // formed by this call's first kernel
   if (splits == 1) {
     ga.kv = reinterpret_cast<const uint16_t*>(part);
   } else {

@@ -53,11 +53,13 @@ class EngramLayer:
     kept alive by this object.  table and scale may instead be pinned host
     tensors (``pin_memory()``): the gather then reads them in place over the
     host link, the layer runs on ``device`` (default: the current CUDA
-    device)."""
+    device).  With ``row_offset`` the table is one shard of a row-split table:
+    it holds global rows [row_offset, row_offset + R), and every other id
+    gives a zero row (see EngramShard)."""
 
     def __init__(self, table, scale, wkv, q_weight, k_weight, *, dim=5120, hc_mult=4, n_cols=24, head_dim=256,
                  scale_block=128, scale_fmt=_lib.SCALE_F32, eps=1e-6, clamp=1e-6, max_tokens=4096,
-                 check_ids=False, fuse_gate=False, wkv_scale=None, device=None):
+                 check_ids=False, fuse_gate=False, wkv_scale=None, device=None, row_offset=0):
         if table.device.type == "cuda":
             dev = table.device
         elif table.is_pinned():
@@ -90,7 +92,7 @@ class EngramLayer:
         self.cfg = EngramConfig(dim=dim, hc_mult=hc_mult, n_cols=n_cols, head_dim=head_dim,
                                 scale_block=scale_block, scale_fmt=scale_fmt, num_rows=R, eps=eps, clamp=clamp,
                                 max_tokens=max_tokens, check_ids=1 if check_ids else 0,
-                                fuse_gate=1 if fuse_gate else 0, wkv_fmt=wkv_fmt)
+                                fuse_gate=1 if fuse_gate else 0, wkv_fmt=wkv_fmt, row_offset=row_offset)
         w = EngramWeights(table=_ptr(table), scale=_ptr(scale), wkv=_ptr(wkv), q_weight=_ptr(q_weight),
                           k_weight=_ptr(k_weight), wkv_scale=_ptr(wkv_scale))
         self._ctx = ctypes.c_void_p()
@@ -160,6 +162,21 @@ class EngramLayer:
               "engram_lookup")
         return rows
 
+    def forward_rows(self, rows, x, token_mask=None, out=None, stream=None):
+        """out = Engram(x) from gathered rows [B, T, n_cols*head_dim] bf16 (as
+        lookup() writes them, or their sum over the shards of a row-split
+        table); out may be x."""
+        B, T = x.shape[0], x.shape[1]
+        _need(rows, "rows", _U16, (B, T, self.K), self.device)
+        _need(x, "x", _U16, (B, T, self.hc_mult, self.dim), self.device)
+        m = self._mask(token_mask, B, T)
+        if out is None:
+            out = torch.empty_like(x)
+        _need(out, "out", _U16, tuple(x.shape), self.device)
+        check(self._lib.engram_forward_rows(self._ctx, _ptr(rows), _ptr(x), _ptr(m), _ptr(out), B, T,
+                                            _stream(stream)), "engram_forward_rows")
+        return out
+
     def sync_status(self, stream=None):
         """(status, bad_ids): waits for the stream, returns and clears the
         device-detected error."""
@@ -202,6 +219,77 @@ class EngramLayer:
             self.close()
         except Exception:
             pass
+
+
+def shard_rows(num_rows: int, rank: int, world_size: int) -> tuple[int, int]:
+    """Rows [start, end) of the table that `rank` of `world_size` holds when
+    the table is split by rows the way `ParallelEngramEmbedding` splits it
+    (atlas.klimoza.dev "deepseek-v4.1 / engram-second"): P = ceil(R /
+    world_size) rows per rank, rank r from r*P.  The last shard ends at R
+    (the excerpt's last part is padded to P rows that no id reaches)."""
+    if world_size < 1 or not 0 <= rank < world_size or num_rows < 0:
+        raise ValueError("need 0 <= rank < world_size and num_rows >= 0")
+    part = -(-num_rows // world_size)
+    start = min(rank * part, num_rows)
+    return start, min(start + part, num_rows)
+
+
+def exchange_rows(rows: torch.Tensor, group=None) -> torch.Tensor:
+    """The one exchange of the row-split layer, in place: every rank's
+    gathered rows (zero for ids outside its shard) summed over the ranks of
+    `group`, the `dist.all_reduce` of `ParallelEngramEmbedding.forward`.  The
+    sum runs on the rows' bit patterns as 32-bit integers: exactly one rank
+    holds each row and the others hold zero bits, so the sum is that rank's
+    bits exactly -- including -0.0, which a floating-point sum would turn into
+    +0.0.  A no-op without an initialised process group of more than one
+    rank.  Collective: every rank of the group must call it."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size(group) == 1:
+        return rows
+    if rows.element_size() * rows.numel() % 4 != 0 or not rows.is_contiguous():
+        raise ValueError("rows must be contiguous and a whole number of 32-bit words")
+    dist.all_reduce(rows.view(torch.int32), op=dist.ReduceOp.SUM, group=group)
+    return rows
+
+
+class EngramShard:
+    """One rank's part of an Engram layer whose table is split by rows over
+    the ranks of a process group (one GPU per rank), as `ParallelEngramEmbedding`
+    splits it: this rank holds rows shard_rows(R, rank, world_size) of the
+    table (table and scale are that shard), wkv and q/k weights whole.
+
+    forward(): engram_lookup on the shard (zero rows for ids outside it) ->
+    exchange_rows (one all-reduce of [B*T, n_cols*head_dim] bf16 over the
+    group) -> engram_forward_rows.  Every rank passes the same hash ids and x
+    and gets the whole layer's output; with one rank it equals
+    EngramLayer.forward bit for bit.  Keyword arguments are EngramLayer's
+    (bf16 weight only)."""
+
+    def __init__(self, table, scale, wkv, q_weight, k_weight, *, num_rows, group=None, **kw):
+        import torch.distributed as dist
+        dist_on = dist.is_available() and dist.is_initialized()
+        self.group = group
+        self.rank = dist.get_rank(group) if dist_on else 0
+        self.world_size = dist.get_world_size(group) if dist_on else 1
+        start, end = shard_rows(num_rows, self.rank, self.world_size)
+        if table.shape[0] != end - start:
+            raise ValueError(f"rank {self.rank} holds rows [{start}, {end}): table has {table.shape[0]} rows")
+        if kw.get("wkv_scale") is not None:
+            raise ValueError("the row-split layer takes the bf16 weight")
+        self.layer = EngramLayer(table, scale, wkv, q_weight, k_weight, row_offset=start, **kw)
+        self.rows_range = (start, end)
+
+    def forward(self, hash_ids, x, token_mask=None, out=None, rows=None):
+        """out = Engram(x), on the current torch stream; rows: optional
+        [B, T, K] bf16 buffer for the exchanged rows."""
+        rows = self.layer.lookup(hash_ids, rows=rows)
+        exchange_rows(rows, self.group)
+        return self.layer.forward_rows(rows, x, token_mask, out=out)
+
+    __call__ = forward
+
+    def close(self):
+        self.layer.close()
 
 
 class EngramHasher:

@@ -117,6 +117,14 @@ typedef struct {
                            wait may run out (ENGRAM_ETIMEOUT) instead of completing. */
   int32_t wkv_fmt;      /* engram_wkv_fmt; ENGRAM_WKV_MXFP8 needs K a multiple of 128 and
                            takes no fused epilogue (fuse_gate is ignored) */
+  int64_t row_offset;   /* global id of the table's first row, >= 0: the table holds rows
+                           [row_offset, row_offset + num_rows) of the whole table, one shard of
+                           a table split by rows over several GPUs, as `ParallelEngramEmbedding`
+                           splits it (atlas.klimoza.dev "deepseek-v4.1 / engram-second": rank r
+                           owns rows [r*P, r*P + P), P = ceil(R / world_size)); 0 for a whole
+                           table.  An id outside the shard gives a zero row (and is counted by
+                           check_ids), so the shards' gathered rows, summed over the ranks, are
+                           the whole table's rows: see engram_forward_rows() */
 } engram_config;
 
 /* table and scale may live in device memory or in host memory that the device
@@ -126,7 +134,9 @@ typedef struct {
  * same kernel, its rows crossing the host link on every call (NVLink-C2C on a
  * Grace-Blackwell node): the pages keep the tables in host memory.  engram_create
  * returns ENGRAM_EINVAL for a table or scale pointer the device cannot read at
- * that address (unregistered host memory, another device's memory). */
+ * that address (unregistered host memory, another device's memory), and so it
+ * does for wkv, wkv_scale, q_weight and k_weight; engram_forward_noalloc()
+ * makes the same checks on every call. */
 typedef struct {
   const uint8_t* table;     /* device or mapped pinned host, [R, head_dim] fp8-e4m3 codes */
   const void* scale;        /* device or mapped pinned host, [R, head_dim/scale_block]
@@ -183,9 +193,27 @@ ENGRAM_API engram_status engram_gate_apply(engram_ctx* ctx, const uint16_t* kv, 
 
 /* Steps 1-3 only: the gathered, dequantised rows, [B*T, n_cols*head_dim] bf16,
  * written to the device buffer rows (the `ParallelEngramEmbedding` output,
- * flattened). */
+ * flattened; on a shard context, before its all-reduce: zero rows for ids
+ * outside the shard). */
 ENGRAM_API engram_status engram_lookup(engram_ctx* ctx, const int64_t* hash_ids, uint16_t* rows,
                             int64_t B, int64_t T, engram_stream_t stream);
+
+/* Steps 4-6 on gathered rows the caller provides: rows [B*T, n_cols*head_dim]
+ * bf16 (device), as engram_lookup() writes them, -> out = layer(x).  This is
+ * the second half of the row-sharded layer: each GPU gathers the rows of its
+ * shard with engram_lookup() (zero rows for ids outside it), the GPUs sum the
+ * rows over the ranks -- the one exchange of the sharded layer, the
+ * `dist.all_reduce` of `ParallelEngramEmbedding.forward` (atlas.klimoza.dev
+ * "deepseek-v4.1 / engram-second"); exactly one rank holds each row, so a sum
+ * of the bit patterns as integers reproduces the rows bit for bit -- and each
+ * GPU then calls engram_forward_rows() on the summed rows.  On rows from
+ * engram_lookup() of the whole table the result equals engram_forward() bit
+ * for bit.  out may equal x.  Takes the bf16 weight only (ENGRAM_EUNSUPPORTED
+ * for ENGRAM_WKV_MXFP8, whose projection reads the table's codes).  rows must
+ * not be written until the call's work on `stream` has finished. */
+ENGRAM_API engram_status engram_forward_rows(engram_ctx* ctx, const uint16_t* rows, const uint16_t* x,
+                                             const uint8_t* token_mask, uint16_t* out, int64_t B, int64_t T,
+                                             engram_stream_t stream);
 
 /* Waits for `stream`, then returns and clears the device-detected error
  * recorded by earlier calls on this context: ENGRAM_ERANGE (with check_ids),
@@ -302,10 +330,16 @@ ENGRAM_API engram_status engram_hash(const engram_hash_config* cfg, const int32_
  *  - cfg and w are as for engram_create() (max_tokens, check_ids and
  *    fuse_gate are ignored); the weights are read on every call.  Shapes with
  *    n_cols*head_dim > 6144 or dim*(hc_mult+1) > 25600 give ENGRAM_EUNSUPPORTED.
- *  - B*T > ENGRAM_NOALLOC_MAX_TOKENS gives ENGRAM_EINVAL and queues nothing.
+ *  - B*T > ENGRAM_NOALLOC_MAX_TOKENS gives ENGRAM_EINVAL and queues nothing;
+ *    so does a table, scale, wkv, q_weight or k_weight pointer that the
+ *    current device cannot read where it is (pageable host memory, another
+ *    device's memory).
  *  - The first call on each device looks up the device address of the scratch
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture on the device.
+ *    before any stream capture on the device.  The address is looked up again
+ *    when the device's context has changed since (after cudaDeviceReset the
+ *    module, and the array with it, is loaded anew); the first call after such
+ *    a reset should therefore also come before any stream capture.
  *  - Every call on a device shares the one scratch array, which keeps the last
  *    call's contents; the call clears the part that must start at zero (the
  *    error word) on `stream` before its kernels run.  Calls that overlap on the

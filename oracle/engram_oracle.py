@@ -151,6 +151,39 @@ def lookup(hash_ids, table, scale, scale_block: int, scale_fmt: int = SCALE_F32)
     return out.reshape(M, C * hd)
 
 
+def shard_bounds(num_rows: int, rank: int, world_size: int):
+    """Rows [start, end) of the table held by `rank` when the table is split
+    by rows over `world_size` ranks, as ``ParallelEngramEmbedding.__init__``
+    splits it: part = ceil(num_rows / world_size) rows per rank, rank r from
+    r*part.  The excerpt's last part may run past the table (its parameter is
+    padded to `part` rows); here it ends at num_rows, since no id of the table
+    reaches past it (an id >= num_rows gives a zero row, as with one rank)."""
+    part = (num_rows + world_size - 1) // world_size
+    start = rank * part
+    return min(start, num_rows), min(start + part, num_rows)
+
+
+def lookup_shard(hash_ids, table_shard, scale_shard, row_start: int, scale_block: int,
+                 scale_fmt: int = SCALE_F32) -> np.ndarray:
+    """One rank's rows before the exchange, as ``ParallelEngramEmbedding.forward``
+    forms them: ids outside [row_start, row_start + shard rows) are masked,
+    every id is made local (id - row_start, masked ones set to 0), the local
+    row is looked up and dequantised, and masked rows are set to zero.
+    Returns bf16 bits [M, n_cols*head_dim]."""
+    ids = np.asarray(hash_ids, dtype=np.int64)
+    M, C = ids.shape
+    table_shard = np.asarray(table_shard, dtype=np.uint8)
+    rows, hd = table_shard.shape
+    mask = (ids < row_start) | (ids >= row_start + rows)
+    local = np.where(mask, 0, ids - row_start)
+    out = np.zeros((M, C, hd), dtype=np.uint16)
+    if rows > 0:
+        vals = dequant_rows(table_shard[local.reshape(-1)], np.asarray(scale_shard)[local.reshape(-1)], scale_block,
+                            scale_fmt).reshape(M, C, hd)
+        out = np.where(mask[:, :, None], np.uint16(0), vals)
+    return out.reshape(M, C * hd)
+
+
 # --------------------------------------------------------------------------
 # a4: projection
 # --------------------------------------------------------------------------

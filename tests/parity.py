@@ -33,12 +33,13 @@ def weight_values(inp: synth.HostInputs) -> np.ndarray:
     return O.mxfp8_weight(inp.wkv, inp.wkv_scale)
 
 
-def kv_bound(e_bits, w_values, kv_ref_bits, K: int, splits: int = 3):
+def kv_bound(e_bits, w_values, kv_ref_bits, K: int, splits: int = 8):
     """Per-element bound on |gpu kv - oracle kv|: one bf16 step at the oracle
     value plus the fp32 dot-product error bound gamma_n * sum_k |e_k W_jk|
     (Higham, "Accuracy and Stability of Numerical Algorithms", section 3.1),
     with n = K/16 accumulator additions of MMA partials (16 or 32 products
-    each), 32 more for the partial itself, and the split-K additions.
+    each), 32 more for the partial itself, and the split-K additions (8, the
+    largest number of K ranges any plan sums).
     w_values: the weight as float64 [N, K] (weight_values)."""
     n = K // 16 + 32 + splits
     u = 2.0 ** -24

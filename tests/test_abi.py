@@ -66,7 +66,7 @@ int main(void) {
   F(engram_config, dim); F(engram_config, hc_mult); F(engram_config, n_cols); F(engram_config, head_dim);
   F(engram_config, scale_block); F(engram_config, scale_fmt); F(engram_config, num_rows); F(engram_config, eps);
   F(engram_config, clamp); F(engram_config, max_tokens); F(engram_config, check_ids); F(engram_config, fuse_gate);
-  F(engram_config, wkv_fmt);
+  F(engram_config, wkv_fmt); F(engram_config, row_offset);
   printf("engram_weights %zu\n", sizeof(engram_weights));
   F(engram_weights, table); F(engram_weights, scale); F(engram_weights, wkv); F(engram_weights, q_weight);
   F(engram_weights, k_weight); F(engram_weights, wkv_scale);
@@ -93,7 +93,7 @@ int main(void) {
 
 def test_host_only_entry_points(libs):
     lib = libs.engram()
-    assert lib.engram_abi_version() == 102
+    assert lib.engram_abi_version() == 103
     for code, text in ((0, b"ok"), (-1, b"invalid argument"), (-4, b"hash id outside the table"),
                        (-5, b"kernel wait timed out"), (-6, b"unsupported shape or format"), (7, b"unknown status")):
         assert lib.engram_status_string(code) == text
@@ -108,6 +108,7 @@ def test_host_only_entry_points(libs):
     assert lib.engram_lookup_project(None, None, None, 1, 1, None) == -1
     assert lib.engram_gate_apply(None, None, None, None, None, None, 1, 1, None) == -1
     assert lib.engram_lookup(None, None, None, 1, 1, None) == -1
+    assert lib.engram_forward_rows(None, None, None, None, None, 1, 1, None) == -1
     assert lib.engram_sync_status(None, None, None) == -1
     assert lib.engram_plan(None, 1, None, None) == -1
     assert lib.engram_set_sm_budget(None, 8) == -1
