@@ -107,6 +107,8 @@ def test_engram_shard_on_a_one_rank_nccl_group(env):
     from engram_hashed_gram_gb300.layer import EngramShard
     if dist.is_initialized():
         pytest.skip("a process group already exists")
+    if not dist.is_nccl_available():
+        pytest.skip("torch.distributed has no NCCL backend here")
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(_free_port())
     dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
