@@ -291,7 +291,7 @@ def config_of(w):
             "table_gb": round(w.num_rows() * w.head_dim / 1e9, 2), "hash_ids": w.ids, "mask": w.mask,
             "prime_base": w.prime_base,
             "wkv": "bf16 [25600, 6144]" if w.wkv_fmt == 0 else "mxfp8 [25600, 6144]: e4m3 + e8m0 per 32 inputs",
-            "table_scales": "fp32 per 128" if w.scale_fmt == 0 else "e8m0 per 32", "fuse_gate": bool(getattr(ARGS, "fuse_gate", False)),
+            "table_scales": "fp32 per 128" if w.scale_fmt == 0 else "e8m0 per 32", "fuse_gate": getattr(ARGS, "fuse_gate", "auto"),
             "table_placement": ("pinned host memory, read in place over the host link"
                                 if getattr(ARGS, "table_host", False) else "device"),
             "l2": L2_NOTE}
@@ -313,7 +313,8 @@ def run_ours(args, w, rank, world, local_rank):
     inp = synth.make_inputs(w)
     table, scale = SD.make_table(w, device=dev, host=args.table_host)
     d = SD.upload_inputs(inp, device=dev)
-    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps, fuse_gate=args.fuse_gate,
+    layer = EngramLayer(table, scale, d["wkv"], d["q"], d["k"], max_tokens=M, eps=w.eps,
+                        fuse_gate={"auto": None, "on": True, "off": False}[args.fuse_gate],
                         device=dev,
                         scale_block=w.scale_block, scale_fmt=w.scale_fmt, wkv_scale=d["wkv_scale"])
     ids, x, mask = d["hash_ids"], d["x"], d["mask"]
@@ -745,8 +746,9 @@ def main():
     ap.add_argument("--table-host", action="store_true",
                     help="keep the table and its scales in pinned host memory (the gather reads them over the "
                          "host link)")
-    ap.add_argument("--fuse-gate", action="store_true",
-                    help="form the gate in the projection's epilogue (engram_config.fuse_gate)")
+    ap.add_argument("--fuse-gate", choices=["auto", "on", "off"], default="auto",
+                    help="where the gate is formed (engram_config.fuse_gate): auto = the library's choice by batch "
+                         "size, on = in the projection's epilogue, off = in a kernel of its own")
     ap.add_argument("--prime-base", type=int, default=None,
                     help="profiling only: build the table from the 24 primes above this base instead of the "
                          "workload's (the projection and gate kernels do the same work; the gather reads a "

@@ -36,6 +36,7 @@ struct engram_ctx {
   float* gsum;                // [max_tokens, hc, dim/256, 4] fused-epilogue block sums
   float* gates;               // [max_tokens, 4] fused-epilogue gates
   uint32_t* counters;         // [ceil(max_tokens/128), 8] fused-epilogue counters and flags
+  uint32_t* tickets;          // [2] fused-epilogue work tickets (0 between launches)
   float* rem_ws;              // [num_sms * 4, 128, 256] remainder-split partial tiles (batches > 128 only)
   uint8_t* wpack;             // wkv in 32 KB swizzled tiles (launch_pack_wkv): N*K*2 bytes, N*K for MXFP8
   bool fp8;                   // MXFP8 weight: block-scaled FP8 projection
@@ -65,6 +66,30 @@ struct Plan {
 };
 
 constexpr int kMaxRemSplits = 4;
+
+// engram_config.fuse_gate: 0 = the library decides by batch size, 1 = the
+// fused gate epilogue whenever the plan allows it, -1 = never.
+constexpr int32_t kFuseAuto = 0;
+constexpr int32_t kFuseAlways = 1;
+
+// Batches of at least this many tokens take the fused gate epilogue when
+// fuse_gate is 0 (ENGRAM_FUSE_MIN overrides it for measurements).
+int64_t fuse_auto_min_tokens() {
+  static const int64_t v = [] {
+    const char* e = std::getenv("ENGRAM_FUSE_MIN");
+    return e != nullptr ? static_cast<int64_t>(std::atoll(e)) : INT64_MAX;
+  }();
+  return v;
+}
+
+// Whether engram_forward over M tokens forms the gate in the projection's
+// epilogue when the plan allows it (bf16 weight, whole-K tiles, shared memory
+// for the fused variant).
+bool wants_fused(const engram_ctx* c, int64_t M) {
+  if (c->fp8 || !gemm_can_fuse(M)) return false;
+  if (c->cfg.fuse_gate >= kFuseAlways) return true;
+  return c->cfg.fuse_gate == kFuseAuto && M >= fuse_auto_min_tokens();
+}
 constexpr int64_t kBulkEpilogueTokens = 2048;
 constexpr int64_t kKeepWeightTokens = 2048;
 
@@ -110,13 +135,13 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
   // a whole tile's K loop: cut those tiles into rem_splits K ranges when that
   // shortens the last wave (each range's fp32 sums go to a workspace; the last
   // range of a tile to finish adds them up in order).  A context with the
-  // fused gate epilogue keeps whole tiles, so that its forward and its
-  // lookup_project + gate_apply sum kv in the same order.
+  // fused gate epilogue (for this batch size) keeps whole tiles, so that its
+  // forward and its lookup_project + gate_apply sum kv in the same order.
   // Only a small last wave is cut (at most a quarter of the grid): measured on
   // GB300, 8 of 152 tiles (4096 tokens) gain 2.5 %, while 96 of 152 (512
   // tokens) lose to the cut tiles' extra epilogues and the reduction.
   const int64_t rem = tiles % sms;
-  if (best == 1 && c->rem_ws != nullptr && !c->cfg.fuse_gate && tiles > sms && rem > 0 && rem <= sms / 4 &&
+  if (best == 1 && c->rem_ws != nullptr && !wants_fused(c, M) && tiles > sms && rem > 0 && rem <= sms / 4 &&
       !(forced >= 1 && forced <= kMaxSplits)) {
     int64_t best_rem = kbt;                          // cost of the partial wave as it is
     for (int32_t s = 2; s <= kMaxRemSplits; ++s) {
@@ -183,7 +208,7 @@ struct FusedIO {
   uint16_t* out;
 };
 
-bool fuses(const engram_ctx* c, const Plan& p, int64_t M) { return !c->fp8 && p.splits == 1 && gemm_can_fuse(M); }
+bool fuses(const engram_ctx* c, const Plan& p, int64_t M) { return p.splits == 1 && wants_fused(c, M); }
 
 // gathered rows -> projection.  The rows are gathered from `ids` into the
 // context's buffer, or, with rows_in (bf16 weight only), taken from the
@@ -194,7 +219,7 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* 
                              const FusedIO* fused, Plan* plan_out, cudaStream_t stream) {
   if (cudaSetDevice(c->device) != cudaSuccess) return ENGRAM_ECUDA;
   const Plan p = make_plan(c, M);
-  const bool fuse = fused != nullptr && c->cfg.fuse_gate && fuses(c, p, M);
+  const bool fuse = fused != nullptr && fuses(c, p, M);
   GatherArgs g = gather_args(c, ids, c->rows, M);
   const bool rem = !fuse && p.rem_splits > 0;
   if (fuse) {
@@ -261,6 +286,7 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* 
     a.out = fused->out;
     a.gsum = c->gsum;
     a.counters = c->counters;
+    a.tickets = c->tickets;
     a.gates = c->gates;
     a.key_n_tiles = c->cfg.hc_mult * c->cfg.dim / kBN;
     a.hold_ready_flags = (c->test_hooks & ENGRAM_TEST_HOLD_GATE_FLAGS) != 0 ? 1 : 0;
@@ -309,6 +335,7 @@ void free_ctx(engram_ctx* c) {
   cudaFree(c->err);
   cudaFree(c->gsum);
   cudaFree(c->counters);
+  cudaFree(c->tickets);
   cudaFree(c->gates);
   cudaFree(c->wpack);
   cudaFree(c->rem_ws);
@@ -326,7 +353,7 @@ engram_status forward_from(engram_ctx* ctx, const int64_t* hash_ids, const uint1
   const FusedIO io{x, token_mask, out};
   engram_status st = run_projection(ctx, hash_ids, rows, M, ctx->kv, &io, &p, s);
   if (st != ENGRAM_OK) return st;
-  if (ctx->cfg.fuse_gate && fuses(ctx, p, M)) {   // the projection's epilogue applied the gate
+  if (fuses(ctx, p, M)) {   // the projection's epilogue applied the gate
     mark(ctx, 3, s);
     return ENGRAM_OK;
   }
@@ -429,6 +456,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
             cudaMalloc(&ctx->counters, static_cast<size_t>((mt + kBM - 1) / kBM) * 8 * sizeof(uint32_t)) ==
                 cudaSuccess &&
             cudaMalloc(&ctx->gates, static_cast<size_t>(mt) * 4 * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&ctx->tickets, 2 * sizeof(uint32_t)) == cudaSuccess &&
             cudaMalloc(&ctx->wpack, static_cast<size_t>(N) * K * (fp8 ? 1 : 2)) == cudaSuccess;
   const size_t sfa_bytes = static_cast<size_t>((mt + kBM - 1) / kBM) * (K / 128) * 512;
   if (ok && mt > kSplitMaxTokens)
@@ -444,6 +472,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
     return ENGRAM_ENOMEM;
   }
   if (cudaMemset(ctx->err, 0, 2 * sizeof(unsigned long long)) != cudaSuccess ||
+      cudaMemset(ctx->tickets, 0, 2 * sizeof(uint32_t)) != cudaSuccess ||
       launch_weight_product(w->q_weight, w->k_weight, ctx->wprod, static_cast<int64_t>(hcd), nullptr) !=
           cudaSuccess ||
       (fp8 ? launch_pack_wkv(static_cast<const uint16_t*>(w->wkv), N, K / 2, ctx->wpack, nullptr) != cudaSuccess ||
@@ -605,7 +634,7 @@ engram_status engram_forward_kernels(const engram_ctx* ctx, int64_t m_tokens, in
     return ENGRAM_OK;
   }
   const Plan p = make_plan(ctx, m_tokens);
-  if (ctx->cfg.fuse_gate && fuses(ctx, p, m_tokens)) {
+  if (fuses(ctx, p, m_tokens)) {
     *kernels = 2;                                   // gather, projection with the gate in its epilogue
   } else {
     *kernels = 3 + (p.rem_splits > 0 ? 1 : 0);      // gather, projection, [remainder sums], gate

@@ -74,6 +74,14 @@ constexpr int kEpiGates = 32 * kEpiPitch;            // float [32][4]
 constexpr int kEpiFlags = kEpiGates + 32 * 16;       // int [32]
 constexpr int kEpiWarpBytes = kEpiFlags + 32 * 4;    // 3,200
 
+// Fused mode: the units a CTA works on come from a global ticket counter (see
+// the kernel), and its producer hands each one to the MMA thread and the four
+// epilogue warps through a ring of kRing slots in shared memory: the unit
+// index, a "full" barrier (producer -> consumers) and an "empty" barrier
+// (5 consumer arrivals -> producer).
+constexpr int kRing = 8;
+constexpr int kRingBytes = kRing * 8 + 2 * kRing * 8;
+
 // Per epilogue warp, plain mode: a 32-row x 32-column fp32 tile (pitch 144
 // bytes, so that 16-byte writes of a row per lane and 16-byte reads of 8
 // lanes along a row are both free of bank conflicts).
@@ -90,7 +98,8 @@ struct Cfg {
   static constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
   static constexpr int kEpiOffset = kBarOffset + 256;              // epilogue staging, after the barriers
   static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kEpiOffset + 4 * kPlainWarpBytes;
-  static constexpr size_t kSmemFused = 1024 + kEpiOffset + 4 * kEpiWarpBytes;
+  static constexpr size_t kRingOffset = kEpiOffset + 4 * kEpiWarpBytes;   // fused: the CTA's unit queue
+  static constexpr size_t kSmemFused = 1024 + kRingOffset + kRingBytes;
   static constexpr bool kCanFuse = !FP8 && kSmemFused <= 232448;
   static_assert(!kCanFuse || kSmemFused <= 232448, "fused-mode shared memory");
   static_assert(!FP8 || STAGES * kSfColsPerStage + kSfCol0 <= kTmemCols, "scale columns");
@@ -112,12 +121,47 @@ __device__ __forceinline__ void raster(const GemmArgs& a, int64_t t, int n_count
   mt = gm0 + static_cast<int>(r % gm);
 }
 
-// Unit u -> (M tile, N tile, K split).  In the fused mode every key tile comes
-// before every value tile: a value tile waits only for units with smaller
-// indices, and by the time any CTA reaches the value tiles nearly all key
-// tiles are done.
 __device__ __forceinline__ bool remainder_unit(const GemmArgs& a, int64_t u) {
   return a.rem_splits > 0 && u >= a.full_units;
+}
+
+// Fused mode: unit u -> (M tile, N tile).  The M tiles are taken in groups of
+// group_m; K(g) is the key tiles of group g, V(g) its value tiles, each
+// rasterised with M fastest.  The order is
+//     K(0), K(1), V(0), K(2), V(1), ..., K(G-1), V(G-2), V(G-1)
+// so that a value tile, whose epilogue needs the gates of its rows and so all
+// key tiles of its M tile, comes a whole group of key tiles after them (they
+// are long finished by then), and the value tiles' heavier epilogues (x and
+// out of every stream) are spread over the run instead of bunched at its end.
+// Every unit a value tile waits for has a smaller index.
+__device__ __forceinline__ void fused_coords(const GemmArgs& a, int64_t u, int& mt, int& nt) {
+  const int KT = a.key_n_tiles;
+  const int VT = a.n_tiles - a.key_n_tiles;
+  const int G = (a.m_tiles + a.group_m - 1) / a.group_m;
+  int64_t off = 0;
+  for (int seg = 0; seg < 2 * G; ++seg) {
+    int g;
+    bool key;
+    if (seg == 0) {
+      g = 0, key = true;
+    } else if (seg == 2 * G - 1) {
+      g = G - 1, key = false;
+    } else if (seg & 1) {
+      g = (seg + 1) >> 1, key = true;
+    } else {
+      g = (seg >> 1) - 1, key = false;
+    }
+    const int gm = min(a.group_m, a.m_tiles - g * a.group_m);
+    const int64_t size = static_cast<int64_t>(gm) * (key ? KT : VT);
+    if (u < off + size) {
+      const int64_t l = u - off;
+      mt = g * a.group_m + static_cast<int>(l % gm);
+      nt = static_cast<int>(l / gm) + (key ? 0 : KT);
+      return;
+    }
+    off += size;
+  }
+  mt = 0, nt = 0;   // u >= units: not reached
 }
 
 template <bool FUSED>
@@ -132,13 +176,7 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& m
   sp = static_cast<int>(u % a.splits);
   const int64_t t = u / a.splits;
   if constexpr (FUSED) {
-    const int64_t key_units = static_cast<int64_t>(a.m_tiles) * a.key_n_tiles;
-    if (t < key_units) {
-      raster(a, t, a.key_n_tiles, mt, nt);
-    } else {
-      raster(a, t - key_units, a.n_tiles - a.key_n_tiles, mt, nt);
-      nt += a.key_n_tiles;
-    }
+    fused_coords(a, t, mt, nt);
     return;
   }
   raster(a, t, a.n_tiles, mt, nt);
@@ -511,36 +549,41 @@ __device__ __forceinline__ bool fused_value_epilogue(const GemmArgs& a, uint32_t
                            pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
                            pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
     __syncwarp();
-    uint4 hb[4][kMaxStreams];                        // all of the chunk's x loads in flight together
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4* xr =
-          reinterpret_cast<const uint4*>(a.x + ((m0 + (lane >> 2) + 8 * i) * a.hc) * a.dim + d0 + c * 32 + cg);
+    for (int half = 0; half < 2; ++half) {
+      uint4 hb[2][kMaxStreams];                      // half of the chunk's x loads in flight together
 #pragma unroll
-      for (int s = 0; s < kMaxStreams; ++s)
-        if (flag[i] != 0 && s < a.hc) hb[i][s] = __ldg(xr + s * (a.dim / 8));
-    }
+      for (int ii = 0; ii < 2; ++ii) {
+        const int i = 2 * half + ii;
+        const uint4* xr =
+            reinterpret_cast<const uint4*>(a.x + ((m0 + (lane >> 2) + 8 * i) * a.hc) * a.dim + d0 + c * 32 + cg);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (flag[i] == 0) continue;
-      const int rl = (lane >> 2) + 8 * i;
-      const int64_t mr = m0 + rl;
-      float v[8];
-      unpack8_bf16(*reinterpret_cast<const uint4*>(epi + rl * kEpiPitch + cg * 2), v);
+        for (int s = 0; s < kMaxStreams; ++s)
+          if (flag[i] != 0 && s < a.hc) hb[ii][s] = __ldg(xr + s * (a.dim / 8));
+      }
 #pragma unroll
-      for (int s = 0; s < kMaxStreams; ++s) {
-        if (s >= a.hc) break;
-        uint4 o = hb[i][s];
-        if (flag[i] == 1) {
-          const float gs = gsm[4 * rl + s];
-          float h[8];
-          unpack8_bf16(hb[i][s], h);
-          o.x = pack_bf16x2(fmaf(gs, v[0], h[0]), fmaf(gs, v[1], h[1]));
-          o.y = pack_bf16x2(fmaf(gs, v[2], h[2]), fmaf(gs, v[3], h[3]));
-          o.z = pack_bf16x2(fmaf(gs, v[4], h[4]), fmaf(gs, v[5], h[5]));
-          o.w = pack_bf16x2(fmaf(gs, v[6], h[6]), fmaf(gs, v[7], h[7]));
+      for (int ii = 0; ii < 2; ++ii) {
+        const int i = 2 * half + ii;
+        if (flag[i] == 0) continue;
+        const int rl = (lane >> 2) + 8 * i;
+        const int64_t mr = m0 + rl;
+        float v[8];
+        unpack8_bf16(*reinterpret_cast<const uint4*>(epi + rl * kEpiPitch + cg * 2), v);
+#pragma unroll
+        for (int s = 0; s < kMaxStreams; ++s) {
+          if (s >= a.hc) break;
+          uint4 o = hb[ii][s];
+          if (flag[i] == 1) {
+            const float gs = gsm[4 * rl + s];
+            float h[8];
+            unpack8_bf16(hb[ii][s], h);
+            o.x = pack_bf16x2(fmaf(gs, v[0], h[0]), fmaf(gs, v[1], h[1]));
+            o.y = pack_bf16x2(fmaf(gs, v[2], h[2]), fmaf(gs, v[3], h[3]));
+            o.z = pack_bf16x2(fmaf(gs, v[4], h[4]), fmaf(gs, v[5], h[5]));
+            o.w = pack_bf16x2(fmaf(gs, v[6], h[6]), fmaf(gs, v[7], h[7]));
+          }
+          *reinterpret_cast<uint4*>(a.out + (mr * a.hc + s) * a.dim + d0 + c * 32 + cg) = o;
         }
-        *reinterpret_cast<uint4*>(a.out + (mr * a.hc + s) * a.dim + d0 + c * 32 + cg) = o;
       }
     }
     __syncwarp();                                    // the tile is rewritten by the next chunk
@@ -575,6 +618,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // fused mode: the unit queue (slot values, then the full and empty barriers)
+  volatile int64_t* ring = reinterpret_cast<volatile int64_t*>(smem + (FUSED ? C::kRingOffset : 0));
+  uint64_t* ufull = reinterpret_cast<uint64_t*>(smem + (FUSED ? C::kRingOffset : 0) + kRing * 8);
+  uint64_t* uempty = ufull + kRing;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -589,6 +636,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[b], 4);
     }
     mbar_init(drain, 1);
+    if constexpr (FUSED) {
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(&ufull[i], 1);
+        mbar_init(&uempty[i], 5);   // the MMA thread and the four epilogue warps
+      }
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmA);
@@ -611,14 +664,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued[kStages] = {};
       bool ok = true;
+      // Units: static round-robin (blockIdx.x, + gridDim.x, ...), or, in the
+      // fused mode, tickets from a global counter: a unit is only ever taken
+      // by a running CTA, so a value tile's wait for the key tiles of its M
+      // tile (all with smaller tickets) never depends on a CTA that has not
+      // started.  The producer hands each ticket to the MMA thread and the
+      // epilogue warps through the shared-memory ring (-1: no more units).
+      uint32_t rslot = 0, rphase = 0;
+      auto publish = [&](int64_t v) -> bool {
+        if (!mbar_wait(&uempty[rslot], rphase ^ 1u, abort_flag)) return false;
+        ring[rslot] = v;
+        mbar_arrive(&ufull[rslot]);
+        if (++rslot == kRing) {
+          rslot = 0;
+          rphase ^= 1u;
+        }
+        return true;
+      };
+      int64_t u = blockIdx.x;
+      if constexpr (FUSED) {
+        u = atomicAdd(a.tickets, 1u);
+        publish(u < a.units ? u : -1);            // a fresh ring: no wait
+      }
+      const int64_t first = u;
       // The weight does not depend on the kernel queued before this one (the
       // gather): the first stages of the first unit get their weight tile while
       // the gathered rows are still being written.
       int pre = 0;
-      if (static_cast<int64_t>(blockIdx.x) < a.units) {
+      if (u < a.units) {
         int mt, nt, sp, kf, kn;
-        unit_coords<FUSED>(a, blockIdx.x, mt, nt, sp);
-        unit_kb(a, blockIdx.x, sp, kf, kn);
+        unit_coords<FUSED>(a, u, mt, nt, sp);
+        unit_kb(a, u, sp, kf, kn);
         pre = min(kStages, kn);
         for (int i = 0; i < pre; ++i) {   // fresh ring: every stage is free
           mbar_arrive_expect_tx(&full[i], kStageBytes);
@@ -626,16 +702,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       grid_dependency_wait();     // the gathered rows are written by the gather kernel
-      for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+      while (u < a.units && ok) {
         // the kernel queued after this one (the gate) may start arriving once
         // every CTA has begun its last unit
-        if (u + gridDim.x >= a.units) grid_launch_dependents();
+        if (!FUSED && u + gridDim.x >= a.units) grid_launch_dependents();
         int mt, nt, sp, kb0, kbn;
         unit_coords<FUSED>(a, u, mt, nt, sp);
         unit_kb(a, u, sp, kb0, kbn);
         for (int kb = 0; kb < kbn; ++kb) {
           uint8_t* sf = smSF + stage * C::kSfBytes;
-          if (u == blockIdx.x && kb < pre) {
+          if (u == first && kb < pre) {
             // weight tile already in flight on this stage: add the rows
             load_a<FP8>(a, tmA, smA + stage * kABytes, sf, &full[stage], mt, kb0 + kb, kbt);
           } else {
@@ -652,6 +728,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
+        }
+        if (!ok) break;
+        if constexpr (FUSED) {
+          u = atomicAdd(a.tickets, 1u);
+          if (!publish(u < a.units ? u : -1)) ok = false;
+        } else {
+          u += gridDim.x;
         }
       }
       if (!ok) {
@@ -672,8 +755,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        if (u + gridDim.x >= a.units) grid_launch_dependents();
+      uint32_t rslot = 0, rphase = 0;
+      for (int64_t u = blockIdx.x;; u += gridDim.x) {
+        if constexpr (FUSED) {                       // the producer's next ticket
+          if (!mbar_wait(&ufull[rslot], rphase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          u = ring[rslot];
+          mbar_arrive(&uempty[rslot]);
+          if (++rslot == kRing) {
+            rslot = 0;
+            rphase ^= 1u;
+          }
+          if (u < 0) break;
+        } else {
+          if (u >= a.units) break;
+          if (u + gridDim.x >= a.units) grid_launch_dependents();
+        }
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -740,8 +839,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
-      if (u + gridDim.x >= a.units) grid_launch_dependents();
+    uint32_t rslot = 0, rphase = 0;
+    for (int64_t u = blockIdx.x;; u += gridDim.x) {
+      if constexpr (FUSED) {                         // the producer's next ticket
+        if (!mbar_wait(&ufull[rslot], rphase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        u = ring[rslot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&uempty[rslot]);
+        if (++rslot == kRing) {
+          rslot = 0;
+          rphase ^= 1u;
+        }
+        if (u < 0) break;
+      } else {
+        if (u >= a.units) break;
+        if (u + gridDim.x >= a.units) grid_launch_dependents();
+      }
       int mt, nt, sp;
       unit_coords<FUSED>(a, u, mt, nt, sp);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
@@ -790,6 +906,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if constexpr (FUSED) {
+    // Every CTA has taken its last ticket (before the barrier above); the last
+    // CTA to get here puts the ticket counter back to 0 for the next launch.
+    // The fused kernel never triggers its dependents early (no
+    // griddepcontrol.launch_dependents): the next kernel in the stream, which
+    // may be the next fused projection taking tickets before its own
+    // dependency wait, launches only once every CTA, and so the reset, is done.
+    if (threadIdx.x == 0 && atom_acq_rel_add_u32(a.tickets + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.tickets, 0u);
+      atomicExch(a.tickets + 1, 0u);
+    }
+  }
 }
 
 template <int A_ROWS, int STAGES>

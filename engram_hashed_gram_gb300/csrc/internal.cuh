@@ -131,7 +131,8 @@ struct GemmArgs {
   float* gsum;           // [M, hc, dim/256, 4]: block sums of h^2, key^2, h*w*key
   float* gates;          // [M, 4] the gates of every row, formed by the last key warp of its quarter
   uint32_t* counters;    // [m_tiles, 8]: key tiles done per lane quarter, then gates-ready flags; zeroed by the gather
-  int32_t key_n_tiles;   // n-tiles of the keys (hc*dim/256); every key unit precedes every value unit
+  uint32_t* tickets;     // [2]: the next unit to take, CTAs finished; 0 between launches (the last CTA resets them)
+  int32_t key_n_tiles;   // n-tiles of the keys (hc*dim/256); an M tile's key units precede its value units
   int32_t hold_ready_flags;  // test hook (engram_test_hook): never raise the gates-ready flags
   int32_t dim;
   int32_t hc;

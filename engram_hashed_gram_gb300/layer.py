@@ -55,11 +55,14 @@ class EngramLayer:
     host link, the layer runs on ``device`` (default: the current CUDA
     device).  With ``row_offset`` the table is one shard of a row-split table:
     it holds global rows [row_offset, row_offset + R), and every other id
-    gives a zero row (see EngramShard)."""
+    gives a zero row (see EngramShard).  fuse_gate: None lets the library
+    choose where the gate is formed (in the projection's epilogue or in a
+    kernel of its own) by batch size, True / False force one or the other;
+    the result is the same either way."""
 
     def __init__(self, table, scale, wkv, q_weight, k_weight, *, dim=5120, hc_mult=4, n_cols=24, head_dim=256,
                  scale_block=128, scale_fmt=_lib.SCALE_F32, eps=1e-6, clamp=1e-6, max_tokens=4096,
-                 check_ids=False, fuse_gate=False, wkv_scale=None, device=None, row_offset=0):
+                 check_ids=False, fuse_gate=None, wkv_scale=None, device=None, row_offset=0):
         if table.device.type == "cuda":
             dev = table.device
         elif table.is_pinned():
@@ -92,7 +95,8 @@ class EngramLayer:
         self.cfg = EngramConfig(dim=dim, hc_mult=hc_mult, n_cols=n_cols, head_dim=head_dim,
                                 scale_block=scale_block, scale_fmt=scale_fmt, num_rows=R, eps=eps, clamp=clamp,
                                 max_tokens=max_tokens, check_ids=1 if check_ids else 0,
-                                fuse_gate=1 if fuse_gate else 0, wkv_fmt=wkv_fmt, row_offset=row_offset)
+                                fuse_gate=0 if fuse_gate is None else (1 if fuse_gate else -1), wkv_fmt=wkv_fmt,
+                                row_offset=row_offset)
         w = EngramWeights(table=_ptr(table), scale=_ptr(scale), wkv=_ptr(wkv), q_weight=_ptr(q_weight),
                           k_weight=_ptr(k_weight), wkv_scale=_ptr(wkv_scale))
         self._ctx = ctypes.c_void_p()

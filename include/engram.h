@@ -104,17 +104,19 @@ typedef struct {
   float clamp;          /* lower clamp of |dot| before the square root (1e-6 in V4.1) */
   int32_t max_tokens;   /* largest B*T of any later call; sizes the scratch */
   int32_t check_ids;    /* non-zero: count ids outside [0, R) and report ENGRAM_ERANGE */
-  int32_t fuse_gate;    /* non-zero: when the projection runs without split-K, engram_forward
-                           forms the gate and the residual add in the projection's epilogue
-                           (kv never reaches HBM) instead of a separate kernel.  Same bits
-                           either way; on GB300 the separate kernel measured faster (the
-                           epilogue work slows the power-capped MMA), so 0 is the default.
-                           Such a context keeps whole tiles in its plans (no remainder
-                           split, see engram_plan), so that both ways sum kv alike.  The
-                           value tiles wait for gates that other CTAs of the projection
-                           form, which assumes the whole persistent grid is resident at
-                           once: with kernels of other streams holding SMs meanwhile, a
-                           wait may run out (ENGRAM_ETIMEOUT) instead of completing. */
+  int32_t fuse_gate;    /* where engram_forward forms the gate and the residual add when the
+                           projection runs without split-K: 1 = in the projection's epilogue
+                           (kv never reaches HBM), -1 = in a separate kernel that reads kv,
+                           0 = the library chooses by batch size (the way that measured
+                           faster on GB300).  Same bits either way, and the same as
+                           engram_lookup_project + engram_gate_apply: a batch that takes the
+                           fused epilogue keeps whole tiles in its plan (no remainder split,
+                           see engram_plan), so that both ways sum kv alike.  The fused
+                           projection takes its tiles from a work counter, in an order where
+                           an M tile's key tiles come well before its value tiles, whose
+                           epilogues wait (bounded) for the gates the key tiles form: only
+                           running CTAs take tiles, so the wait never depends on a CTA that
+                           has not started, whatever else shares the GPU. */
   int32_t wkv_fmt;      /* engram_wkv_fmt; ENGRAM_WKV_MXFP8 needs K a multiple of 128 and
                            takes no fused epilogue (fuse_gate is ignored) */
   int64_t row_offset;   /* global id of the table's first row, >= 0: the table holds rows

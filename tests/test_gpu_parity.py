@@ -190,14 +190,17 @@ def test_empty_batch_is_a_no_op(tiny):
     assert layer.sync_status()[0] == 0
 
 
-@pytest.mark.parametrize("B,T,mask_frac", [(1, 150, 0.1), (300, 1, 0.0), (7, 100, 0.3), (64, 1, 0.2), (1, 16, 0.0)])
+@pytest.mark.parametrize("B,T,mask_frac", [(1, 150, 0.1), (300, 1, 0.0), (7, 100, 0.3), (64, 1, 0.2), (1, 16, 0.0),
+                                           (1, 2300, 0.1), (3, 1400, 0.05)])
 def test_fused_epilogue_matches_split_path(tiny, B, T, mask_frac):
     """fuse_gate: the gate and residual add run in the projection's epilogue
     (plans without split-K); the result must equal lookup_project + gate_apply
-    bit for bit, and match the oracle."""
+    bit for bit, and match the oracle.  2,300 and 4,200 tokens span 18 and 33
+    M tiles: several groups of 16 in the fused unit order (key tiles of a
+    group, then the value tiles of the group before), the last one partial."""
     from engram_hashed_gram_gb300.layer import EngramLayer
     dev = tiny["dev"]
-    fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=1024,
+    fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=4200,
                         fuse_gate=True)
     w, inp = _inputs(tiny, B, T, mask_frac, seed=21)
     ids, x, mask = _dev(inp)

@@ -124,7 +124,7 @@ def test_noalloc_matches_forward_and_oracle_v41_shape(env):
 def test_noalloc_matches_forward_and_oracle_split_k(env):
     # dim 512: 10 N tiles fill too little of the grid, so both entry points cut
     # K into 8 ranges and the gate kernel sums the fp32 partials in the scratch
-    _two_calls_in_a_row(env, "dim512", [(48, 1, 3, 0.0), (37, 1, 4, 0.25)], (8, 10))
+    _two_calls_in_a_row(env, "dim512", [(48, 1, 3, 0.0), (37, 1, 4, 0.25)], (8, 80))
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch(env):
