@@ -40,7 +40,6 @@ struct engram_ctx {
   float* rem_ws;              // [num_sms * 4, 128, 256] remainder-split partial tiles (batches > 128 only)
   uint8_t* wpack;             // wkv in 32 KB swizzled tiles (launch_pack_wkv): N*K*2 bytes, N*K for MXFP8
   bool fp8;                   // MXFP8 weight: block-scaled FP8 projection
-  bool table_on_device;       // the table is this device's memory (not host memory)
   uint8_t* wsf;               // fp8: the weight's scales, packed (launch_pack_sfb), N*K/32 bytes
   uint8_t* codes;             // fp8: [max_tokens, K] gathered e4m3 codes
   uint8_t* sfa;               // fp8: [ceil(max_tokens/128), K/128, 512] gathered scales
@@ -198,7 +197,6 @@ GatherArgs gather_args(const engram_ctx* c, const int64_t* ids, uint16_t* out, i
   g.scale_fmt = c->cfg.scale_fmt;
   g.check_ids = c->cfg.check_ids;
   g.err = c->err;
-  g.table_on_device = c->table_on_device ? 1 : 0;
   return g;
 }
 
@@ -437,7 +435,6 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
     delete ctx;
     return ENGRAM_EINVAL;
   }
-  ctx->table_on_device = on_device(w->table, ctx->device);
   int cc_major = 0, cc_minor = 0;
   cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, ctx->device);
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
@@ -482,8 +479,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
                  launch_pack_sfb(w->wkv_scale, N, K, ctx->wsf, nullptr) != cudaSuccess ||
                  cudaMemset(ctx->sfa, 127, sfa_bytes) != cudaSuccess   // scales of rows past M: 1.0
            : launch_pack_wkv(static_cast<const uint16_t*>(w->wkv), N, K, ctx->wpack, nullptr) != cudaSuccess) ||
-      gemm_prepare() != cudaSuccess || gate_prepare() != cudaSuccess || gather_prepare() != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess) {
+      gemm_prepare() != cudaSuccess || gate_prepare() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     free_ctx(ctx);
     return ENGRAM_ECUDA;
   }

@@ -17,9 +17,6 @@
 //
 // gather_codes_kernel serves the MXFP8 weight: it copies the codes unchanged
 // and places the E8M0 scales in the block-scaled projection's order.
-#include <cstdlib>
-#include <cstring>
-
 #include "common.cuh"
 #include "internal.cuh"
 
@@ -90,143 +87,6 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
   }
 }
 
-// ---------------------------------------------------------------- staged gather
-// The same rows and bits as gather_dequant_kernel, with the table rows staged
-// through shared memory by the copy engine.  Each warp takes batches of 32
-// rows: lane l reads the id of row l of the batch (one coalesced load for the
-// warp), issues one bulk copy (cp.async.bulk) of that row's codes into the
-// warp's slot -- all 32 copies counted on one mbarrier -- and loads the row's
-// scales (at most 16 bytes) into registers.  While a batch is in flight the
-// warp dequantises the previous one from shared memory (two slots per warp):
-// lanes 16h..16h+15 cover one row's 16 chunks of 16 codes, taking the row's
-// scales from its lane by shuffle, so each store instruction writes two whole
-// bf16 rows.  No thread waits on a chain of dependent loads of its own, and an
-// SM keeps up to 16 batches (128 KB of codes) in flight.  Used for a table in
-// the device's own memory, head_dim <= 256, a 16-byte-aligned table and
-// 4-byte scale words per row; other tables take gather_dequant_kernel.
-constexpr int kStagedWarps = 8;
-constexpr int kStagedSlotBytes = 32 * 256;
-constexpr int kStagedSmem = kStagedWarps * 2 * kStagedSlotBytes + kStagedWarps * 2 * 8;
-
-template <int SCALE_FMT>
-__global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(GatherArgs a) {
-  extern __shared__ __align__(128) uint8_t gsm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* slots = gsm + warp * 2 * kStagedSlotBytes;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(gsm + kStagedWarps * 2 * kStagedSlotBytes) + warp * 2;
-  if (lane == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbarrier_init();
-  }
-  __syncwarp();
-  grid_dependency_wait();        // the ids may come from the previous kernel
-  grid_launch_dependents();      // let the projection start its weight stream
-  if (a.zero != nullptr) {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero; i += gridDim.x * blockDim.x) a.zero[i] = 0u;
-  }
-  const int nb = a.head_dim / a.scale_block;
-  const int swords = (nb * (SCALE_FMT == 0 ? 4 : 1)) >> 2;   // 32-bit scale words per row (1..4)
-  const int cpr = a.head_dim >> 4;                           // 16-byte chunks per row
-  const int64_t batches = (a.rows_total + 31) >> 5;
-  const int64_t wstride = static_cast<int64_t>(gridDim.x) * kStagedWarps;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kStagedWarps + warp;
-  const uint32_t* scale_words = static_cast<const uint32_t*>(a.scale);
-  const uint64_t pol = policy_evict_first();
-
-  // per slot (two named copies, so that they stay in registers): the rows of
-  // the batch with an id inside the table, and lane l's scale words of row l
-  uint32_t vmask0 = 0u, vmask1 = 0u;
-  uint32_t sw0[4] = {0u, 0u, 0u, 0u}, sw1[4] = {0u, 0u, 0u, 0u};
-  auto issue = [&](int64_t b, int slot) {
-    const int64_t row = (b << 5) + lane;
-    bool valid = false;
-    uint64_t ur = 0;
-    if (row < a.rows_total) {
-      ur = static_cast<uint64_t>(__ldg(a.ids + row)) - static_cast<uint64_t>(a.row0);
-      valid = ur < static_cast<uint64_t>(a.R);
-      if (!valid && a.check_ids) {
-        atomicAdd(a.err + 1, 1ull);
-        atomicOr(a.err, kErrRange);
-      }
-    }
-    const uint32_t vm = __ballot_sync(0xFFFFFFFFu, valid);
-    if (slot) vmask1 = vm; else vmask0 = vm;
-    const uint32_t total = static_cast<uint32_t>(__popc(vm)) * static_cast<uint32_t>(a.head_dim);
-    if (lane == 0) mbar_arrive_expect_tx(&bar[slot], total);
-    __syncwarp();
-    if (valid) {
-      bulk_load_hint(slots + slot * kStagedSlotBytes + lane * a.head_dim,
-                     a.table + static_cast<int64_t>(ur) * a.head_dim, static_cast<uint32_t>(a.head_dim), &bar[slot],
-                     pol);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t v = q < swords ? __ldg(scale_words + static_cast<int64_t>(ur) * swords + q) : 0u;
-        if (slot) sw1[q] = v; else sw0[q] = v;
-      }
-    }
-  };
-
-  uint32_t phase[2] = {0u, 0u};
-  uint32_t armed[2] = {0u, 0u};  // copies issued into each slot and not yet waited for
-  bool ok = true;
-  int slot = 0;
-  if (first < batches) {
-    issue(first, 0);
-    armed[0] = 1u;
-  }
-  for (int64_t b = first; b < batches; b += wstride, slot ^= 1) {
-    if (b + wstride < batches) {
-      fence_proxy_async_shared();   // this warp's earlier reads of the slot precede the copies into it
-      issue(b + wstride, slot ^ 1);
-      armed[slot ^ 1] = 1u;
-    }
-    if (!mbar_wait(&bar[slot], phase[slot], nullptr)) {
-      ok = false;
-      break;
-    }
-    phase[slot] ^= 1u;
-    armed[slot] = 0u;
-    const uint8_t* base = slots + slot * kStagedSlotBytes;
-    for (int j = 0; j < 32 * cpr; j += 32) {
-      const int t = j + lane;
-      const int r = t / cpr;                       // row of the batch
-      const int ch = t - r * cpr;
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) w[q] = __shfl_sync(0xFFFFFFFFu, slot ? sw1[q] : sw0[q], r);
-      const int64_t row = (b << 5) + r;
-      if (row >= a.rows_total) continue;
-      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
-      if ((((slot ? vmask1 : vmask0) >> r) & 1u) != 0u) {
-        const uint4 c = ld_shared_v4(smem_u32(base + r * a.head_dim + ch * 16));
-        const int blk = (ch * 16) / a.scale_block;
-        float sc;
-        if (SCALE_FMT == 0) {
-          sc = __uint_as_float(blk == 0 ? w[0] : blk == 1 ? w[1] : blk == 2 ? w[2] : w[3]);
-        } else {
-          const uint32_t word = (blk >> 2) == 0 ? w[0] : (blk >> 2) == 1 ? w[1] : (blk >> 2) == 2 ? w[2] : w[3];
-          sc = e8m0_to_float((word >> (8 * (blk & 3))) & 0xFFu);
-        }
-        dequant4(c.x, sc, lo.x, lo.y);
-        dequant4(c.y, sc, lo.z, lo.w);
-        dequant4(c.z, sc, hi.x, hi.y);
-        dequant4(c.w, sc, hi.z, hi.w);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(a.out + row * a.head_dim + ch * 16);
-      dst[0] = lo;
-      dst[1] = hi;
-    }
-    __syncwarp();                                   // the slot is free for the batch after next
-  }
-  if (!ok) {
-    if (lane == 0) atomicOr(a.err, kErrTimeout);
-    // let the copies in flight land before the CTA can exit
-    for (int i = 0; i < 2; ++i)
-      if (armed[i]) mbar_wait(&bar[i], phase[i], nullptr, kDrainLimitNs);
-  }
-}
-
 // One thread per 16-byte chunk of a row's codes; the first head_dim/32
 // threads of a row also place its scales.
 __global__ void __launch_bounds__(256) gather_codes_kernel(GatherArgs a, int n_cols, int64_t kbt,
@@ -266,15 +126,6 @@ __global__ void __launch_bounds__(256) gather_codes_kernel(GatherArgs a, int n_c
   }
 }
 
-// The staged kernel unless ENGRAM_GATHER=plain (measurements).
-bool staged_gather_enabled() {
-  static const bool on = [] {
-    const char* e = std::getenv("ENGRAM_GATHER");
-    return !(e != nullptr && std::strcmp(e, "plain") == 0);
-  }();
-  return on;
-}
-
 }  // namespace
 
 cudaError_t launch_gather_codes(const GatherArgs& a, int n_cols, uint8_t* codes, uint8_t* sfa, int num_sms,
@@ -290,33 +141,9 @@ cudaError_t launch_gather_codes(const GatherArgs& a, int n_cols, uint8_t* codes,
                     K / 128, codes, sfa);
 }
 
-bool staged_gather_fits(const GatherArgs& a) {
-  const int nb = a.head_dim / a.scale_block;
-  const int sbytes = nb * (a.scale_fmt == 0 ? 4 : 1);
-  return a.table_on_device && a.head_dim <= 256 && a.head_dim % 16 == 0 && sbytes % 4 == 0 && sbytes <= 16 &&
-         (reinterpret_cast<uintptr_t>(a.table) & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.scale) & 3u) == 0;
-}
-
-cudaError_t gather_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(gather_staged_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kStagedSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gather_staged_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmem);
-  return e;
-}
-
 cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream) {
   const int64_t total = a.rows_total * (a.head_dim >> 4);
   if (total == 0) return cudaSuccess;
-  if (staged_gather_enabled() && staged_gather_fits(a)) {
-    const int64_t batches = (a.rows_total + 31) / 32;
-    int64_t blocks = (batches + kStagedWarps - 1) / kStagedWarps;
-    if (blocks > num_sms) blocks = num_sms;
-    const dim3 grid(static_cast<unsigned>(blocks));
-    if (a.scale_fmt == 0)
-      return launch_pdl(gather_staged_kernel<0>, grid, dim3(kStagedWarps * 32), kStagedSmem, stream, 1, a);
-    return launch_pdl(gather_staged_kernel<1>, grid, dim3(kStagedWarps * 32), kStagedSmem, stream, 1, a);
-  }
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // 8 resident CTAs of 256 per SM

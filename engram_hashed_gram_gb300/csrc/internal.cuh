@@ -44,16 +44,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // only; it allocates nothing and queues nothing.  A pointer that fails it
 // (pageable host memory, another device's memory) would make the first kernel
 // that dereferences it fault.
-// Whether p is memory of `device` itself (not managed, not host memory).
-inline bool on_device(const void* p, int device) {
-  cudaPointerAttributes at{};
-  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return at.type == cudaMemoryTypeDevice && at.device == device;
-}
-
 inline bool device_readable(const void* p, int device) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -84,10 +74,7 @@ struct GatherArgs {
   unsigned long long* err;  // [0]: flags, [1]: count of ids out of range
   uint32_t* zero;           // words the kernel that follows needs cleared (may be null)
   int32_t n_zero;
-  int32_t table_on_device;  // the table is memory of the device itself: the rows may be staged by
-                            // bulk copies (a table in host memory is read by plain loads)
 };
-cudaError_t gather_prepare();   // per-device one-time kernel attributes
 cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream);
 // MXFP8 operands for the block-scaled projection: the rows' e4m3 codes copied
 // to codes [M, K] (a zero row for an id outside [0, R)) and their E8M0 scales

@@ -200,9 +200,8 @@ extern "C" engram_status engram_forward_noalloc(const engram_config* cfg, const 
   g.scale_block = c.scale_block;
   g.scale_fmt = c.scale_fmt;
   g.check_ids = 0;
-  g.table_on_device = on_device(w->table, dev) ? 1 : 0;
   g.err = err;
-  if (gather_prepare() != cudaSuccess || launch_gather(g, sms, s) != cudaSuccess) return ENGRAM_ECUDA;
+  if (launch_gather(g, sms, s) != cudaSuccess) return ENGRAM_ECUDA;
 
   CUtensorMap tmB;
   if (!make_tmap_bf16(&tmB, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN)) return ENGRAM_ECUDA;
