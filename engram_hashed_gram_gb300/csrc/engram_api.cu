@@ -37,7 +37,6 @@ struct engram_ctx {
   float* gates;               // [max_tokens, 4] fused-epilogue gates
   uint32_t* counters;         // [ceil(max_tokens/128), 8] fused-epilogue counters and flags
   uint32_t* tickets;          // [2] fused-epilogue work tickets (0 between launches)
-  uint32_t* sk_count;         // [num_sms * 4] stream-K parts finished (batches > 128 only)
   float* rem_ws;              // [num_sms * 4, 128, 256] remainder-split partial tiles (batches > 128 only)
   uint8_t* wpack;             // wkv in 32 KB swizzled tiles (launch_pack_wkv): N*K*2 bytes, N*K for MXFP8
   bool fp8;                   // MXFP8 weight: block-scaled FP8 projection
@@ -64,7 +63,6 @@ struct Plan {
   int64_t units;
   int32_t rem_tiles;    // tiles of the partial last wave cut into K ranges (0: none)
   int32_t rem_splits;
-  int32_t sk_groups;    // stream-K groups of m_tiles CTAs (0: none)
 };
 
 constexpr int kMaxRemSplits = 4;
@@ -92,15 +90,6 @@ bool wants_fused(const engram_ctx* c, int64_t M) {
   if (c->cfg.fuse_gate >= kFuseAlways) return true;
   return c->cfg.fuse_gate == kFuseAuto && M >= fuse_auto_min_tokens();
 }
-// Stream-K plans unless ENGRAM_STREAMK=0 (measurements).
-bool streamk_enabled() {
-  static const bool on = [] {
-    const char* e = std::getenv("ENGRAM_STREAMK");
-    return !(e != nullptr && std::atoi(e) == 0);
-  }();
-  return on;
-}
-
 constexpr int64_t kBulkEpilogueTokens = 2048;
 constexpr int64_t kKeepWeightTokens = 2048;
 
@@ -142,20 +131,6 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
     best = forced;
   p.splits = best;
   p.units = tiles * best;
-  // Stream-K for a few M tiles whose whole tiles fill the grid's waves badly
-  // (512 tokens: 400 tiles on 152 SMs are three waves, the last 63% full):
-  // groups of m_tiles CTAs share out the (N tile, K block) steps evenly, each
-  // CTA of a group on its own M tile, so the group streams each weight tile
-  // once.  Needs every group to cover at least one whole tile's K blocks.  A
-  // batch with the fused gate epilogue keeps whole tiles (as below).
-  const int64_t groups = sms / p.m_tiles;
-  const bool sk_ok = best == 1 && c->sk_count != nullptr && !c->fp8 && !wants_fused(c, M) && p.m_tiles <= 8 &&
-                     groups >= 2 && p.n_tiles >= groups && tiles > sms && !(forced >= 1 && forced <= kMaxSplits);
-  if (sk_ok && streamk_enabled() && tiles * 10 < waves(tiles) * sms * 9) {
-    p.sk_groups = static_cast<int32_t>(groups);
-    p.ctas = static_cast<int32_t>(groups * p.m_tiles);
-    return p;
-  }
   // Without split-K, a last wave of rem < sms tiles would leave SMs idle for
   // a whole tile's K loop: cut those tiles into rem_splits K ranges when that
   // shortens the last wave (each range's fp32 sums go to a workspace; the last
@@ -250,15 +225,12 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* 
   if (fuse) {
     g.zero = c->counters;
     g.n_zero = p.m_tiles * 8;
-  } else if (p.sk_groups > 0) {
-    g.zero = c->sk_count;
-    g.n_zero = (p.sk_groups - 1) * p.m_tiles * 4;
   }
   mark(c, 0, stream);
   if (rows_in != nullptr) {
-    // no gather: clear what it would have cleared
-    if (g.zero != nullptr &&
-        cudaMemsetAsync(g.zero, 0, static_cast<size_t>(g.n_zero) * sizeof(uint32_t), stream) != cudaSuccess)
+    // no gather: clear what it would have cleared for the fused epilogue
+    if (fuse && cudaMemsetAsync(c->counters, 0, static_cast<size_t>(p.m_tiles) * 8 * sizeof(uint32_t), stream) !=
+                    cudaSuccess)
       return ENGRAM_ECUDA;
   } else if (c->fp8) {
     if (launch_gather_codes(g, c->cfg.n_cols, c->codes, c->sfa, c->num_sms, stream) != cudaSuccess)
@@ -286,10 +258,6 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* 
     a.rem_ws = c->rem_ws;
   } else if (fuse) {
     a.units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  } else if (p.sk_groups > 0) {
-    a.sk_groups = p.sk_groups;
-    a.sk_ws = c->rem_ws;
-    a.sk_count = c->sk_count;
   }
   a.out_mode = p.splits == 1 ? kOutBf16 : kOutPartial;
   a.kv = kv_out;
@@ -368,7 +336,6 @@ void free_ctx(engram_ctx* c) {
   cudaFree(c->gsum);
   cudaFree(c->counters);
   cudaFree(c->tickets);
-  cudaFree(c->sk_count);
   cudaFree(c->gates);
   cudaFree(c->wpack);
   cudaFree(c->rem_ws);
@@ -494,8 +461,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
   const size_t sfa_bytes = static_cast<size_t>((mt + kBM - 1) / kBM) * (K / 128) * 512;
   if (ok && mt > kSplitMaxTokens)
     ok = cudaMalloc(&ctx->rem_ws, static_cast<size_t>(ctx->num_sms) * kMaxRemSplits * kBM * kBN * sizeof(float)) ==
-             cudaSuccess &&
-         cudaMalloc(&ctx->sk_count, static_cast<size_t>(ctx->num_sms) * 4 * sizeof(uint32_t)) == cudaSuccess;
+         cudaSuccess;
   if (ok && fp8)
     ok = cudaMalloc(&ctx->wsf, static_cast<size_t>(N) * (K / 32)) == cudaSuccess &&
          cudaMalloc(&ctx->codes, static_cast<size_t>(mt) * K) == cudaSuccess &&

@@ -47,8 +47,12 @@ __device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& o0, uint
   o1 = pack_bf16x2(__fmul_rn(f23.x, s), __fmul_rn(f23.y, s));
 }
 
-template <int SCALE_FMT>
-__global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
+// SHIFT: head_dim / 16 and scale_block are powers of two (cpr_log2,
+// sb_log2), and the chunk count fits 32 bits: the index arithmetic is shifts
+// and 32-bit adds instead of 64-bit divisions, which took half the kernel's
+// issue slots.
+template <int SCALE_FMT, bool SHIFT>
+__global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a, int cpr_log2, int sb_log2) {
   grid_dependency_wait();        // the ids may come from the previous kernel
   grid_launch_dependents();      // let the projection start its weight stream
   if (a.zero != nullptr) {
@@ -59,14 +63,22 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(GatherArgs a) {
   const int64_t total = a.rows_total * cpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t row = i / cpr;
-    const int ch = static_cast<int>(i - row * cpr);
+    int64_t row;
+    int ch;
+    if (SHIFT) {
+      const uint32_t i32 = static_cast<uint32_t>(i);
+      row = static_cast<int64_t>(i32 >> cpr_log2);
+      ch = static_cast<int>(i32 & ((1u << cpr_log2) - 1u));
+    } else {
+      row = i / cpr;
+      ch = static_cast<int>(i - row * cpr);
+    }
     const uint64_t ur = static_cast<uint64_t>(__ldg(a.ids + row)) - static_cast<uint64_t>(a.row0);
     const int64_t r = static_cast<int64_t>(ur);
     uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
     if (ur < static_cast<uint64_t>(a.R)) {
       const uint4 c = ld_stream_v4(a.table + r * a.head_dim + ch * 16);
-      const int blk = (ch * 16) / a.scale_block;
+      const int blk = SHIFT ? (ch * 16) >> sb_log2 : (ch * 16) / a.scale_block;
       float s;
       if (SCALE_FMT == 0) {
         s = __ldg(static_cast<const float*>(a.scale) + r * nb + blk);
@@ -149,8 +161,17 @@ cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t stream)
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // 8 resident CTAs of 256 per SM
   if (blocks > cap) blocks = cap;
   const dim3 grid(static_cast<unsigned>(blocks));
-  if (a.scale_fmt == 0) return launch_pdl(gather_dequant_kernel<0>, grid, dim3(threads), 0, stream, 1, a);
-  return launch_pdl(gather_dequant_kernel<1>, grid, dim3(threads), 0, stream, 1, a);
+  const int cpr = a.head_dim >> 4;
+  const int cl = __builtin_ctz(static_cast<unsigned>(cpr));
+  const int sl = __builtin_ctz(static_cast<unsigned>(a.scale_block));
+  const bool shift = (1 << cl) == cpr && (1 << sl) == a.scale_block && total + static_cast<int64_t>(blocks) * threads <
+                                                                           (int64_t{1} << 32);
+  if (shift) {
+    if (a.scale_fmt == 0) return launch_pdl(gather_dequant_kernel<0, true>, grid, dim3(threads), 0, stream, 1, a, cl, sl);
+    return launch_pdl(gather_dequant_kernel<1, true>, grid, dim3(threads), 0, stream, 1, a, cl, sl);
+  }
+  if (a.scale_fmt == 0) return launch_pdl(gather_dequant_kernel<0, false>, grid, dim3(threads), 0, stream, 1, a, 0, 0);
+  return launch_pdl(gather_dequant_kernel<1, false>, grid, dim3(threads), 0, stream, 1, a, 0, 0);
 }
 
 }  // namespace engram

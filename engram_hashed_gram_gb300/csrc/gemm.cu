@@ -193,58 +193,6 @@ __device__ __forceinline__ void unit_kb(const GemmArgs& a, int64_t u, int sp, in
   }
 }
 
-// What one unit of a CTA's work is: output tile (mt, nt), K blocks [kb0,
-// kb0 + kbn), and how its result leaves the epilogue.
-struct Unit {
-  int mt, nt;
-  int sp;        // split-K index, or the K range of a remainder unit
-  int kb0, kbn;
-  bool rem;      // a remainder unit (fp32 sums to rem_ws)
-  int part;      // stream-K: -1 = a whole tile; 0 / 1 = the first / second part of a tile
-  int bnd;       //   cut at group boundary bnd
-};
-
-// Stream-K (a.sk_groups > 0): the sk_groups * m_tiles CTAs form sk_groups
-// groups of m_tiles.  Over the sequence of W = n_tiles * kbt (N tile, K
-// block) steps, N tile major, group g covers [g*W/G, (g+1)*W/G) and CTA i of
-// the group computes M tile i over it, so the m_tiles CTAs of a group stream
-// the same weight tiles at the same time and share them in L2.  The steps of a
-// group fall into segments, one per N tile; a segment that is not a whole
-// tile is one of the two parts of a tile cut at a group boundary (each group
-// covers at least one whole tile's K blocks, so no tile is cut twice).  Unit
-// u of CTA c is its segment (u - c) / gridDim.x.
-template <bool FUSED>
-__device__ __forceinline__ bool unit_at(const GemmArgs& a, int64_t u, int kbt, Unit& t) {
-  t.rem = false;
-  t.part = -1;
-  t.bnd = 0;
-  if (!FUSED && a.sk_groups > 0) {
-    const int cta = static_cast<int>(u % gridDim.x);
-    const int64_t j = u / gridDim.x;
-    const int g = cta / a.m_tiles;
-    const int64_t W = static_cast<int64_t>(a.n_tiles) * kbt;
-    const int64_t s1 = W * (g + 1) / a.sk_groups;
-    int64_t st = W * g / a.sk_groups;
-    for (int64_t k = 0; k < j && st < s1; ++k) st = min(s1, (st / kbt + 1) * kbt);   // the next segment
-    if (st >= s1) return false;
-    t.mt = cta - g * a.m_tiles;
-    t.nt = static_cast<int>(st / kbt);
-    t.kb0 = static_cast<int>(st - static_cast<int64_t>(t.nt) * kbt);
-    t.kbn = static_cast<int>(min(s1, static_cast<int64_t>(t.nt + 1) * kbt) - st);
-    t.sp = 0;
-    if (t.kbn < kbt) {
-      t.part = t.kb0 == 0 ? 0 : 1;
-      t.bnd = t.part == 0 ? g : g - 1;
-    }
-    return true;
-  }
-  if (u >= a.units) return false;
-  unit_coords<FUSED>(a, u, t.mt, t.nt, t.sp);
-  unit_kb(a, u, t.sp, t.kb0, t.kbn);
-  t.rem = !FUSED && remainder_unit(a, u);
-  return true;
-}
-
 // The weight tile (N tile nt, K block kb) into a B stage: one contiguous 32 KB
 // copy from the packed weight, or a 2-D tensor copy of the row-major weight.
 // FP8: the tile's scales (1 KB, packed the same way) go to the stage's B-scale
@@ -413,41 +361,6 @@ __device__ __forceinline__ void bf16_epilogue_release_first(const GemmArgs& a, u
       }
     }
     __syncwarp();                                    // the tile is rewritten by the next chunk
-  }
-}
-
-// Stream-K: the warp's 32 rows of a tile cut at a group boundary, once both
-// parts' fp32 sums are in the workspace (ws: part 0, then part 1, each
-// [128, 256]): kv = bf16(part 0 + part 1), a single fp32 addition, so the
-// result does not depend on which part finished first.  Lane l takes columns
-// 8l .. 8l+7 of a row, 4 rows at a time.
-__device__ __forceinline__ void streamk_finish(const GemmArgs& a, const float* ws, int64_t m0, int q, int nt,
-                                               int lane) {
-  const float* p0 = ws + static_cast<int64_t>(q * 32) * kBN + lane * 8;
-  const float* p1 = p0 + kBM * kBN;
-#pragma unroll 1
-  for (int r0 = 0; r0 < 32; r0 += 4) {
-    float4 x[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t off = static_cast<int64_t>(r0 + i) * kBN;
-      x[i][0] = __ldcg(reinterpret_cast<const float4*>(p0 + off));
-      x[i][1] = __ldcg(reinterpret_cast<const float4*>(p0 + off) + 1);
-      x[i][2] = __ldcg(reinterpret_cast<const float4*>(p1 + off));
-      x[i][3] = __ldcg(reinterpret_cast<const float4*>(p1 + off) + 1);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t m = m0 + r0 + i;
-      if (m >= a.M) break;
-      const float4 lo = make_float4(x[i][0].x + x[i][2].x, x[i][0].y + x[i][2].y, x[i][0].z + x[i][2].z,
-                                    x[i][0].w + x[i][2].w);
-      const float4 hi = make_float4(x[i][1].x + x[i][3].x, x[i][1].y + x[i][3].y, x[i][1].z + x[i][3].z,
-                                    x[i][1].w + x[i][3].w);
-      *reinterpret_cast<uint4*>(a.kv + m * a.N + nt * kBN + lane * 8) =
-          make_uint4(pack_bf16x2(lo.x, lo.y), pack_bf16x2(lo.z, lo.w), pack_bf16x2(hi.x, hi.y),
-                     pack_bf16x2(hi.z, hi.w));
-    }
   }
 }
 
@@ -774,27 +687,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         publish(u < a.units ? u : -1);            // a fresh ring: no wait
       }
       const int64_t first = u;
-      Unit t;
-      bool have = unit_at<FUSED>(a, u, kbt, t);
       // The weight does not depend on the kernel queued before this one (the
       // gather): the first stages of the first unit get their weight tile while
       // the gathered rows are still being written.
       int pre = 0;
-      if (have) {
-        pre = min(kStages, t.kbn);
+      if (u < a.units) {
+        int mt, nt, sp, kf, kn;
+        unit_coords<FUSED>(a, u, mt, nt, sp);
+        unit_kb(a, u, sp, kf, kn);
+        pre = min(kStages, kn);
         for (int i = 0; i < pre; ++i) {   // fresh ring: every stage is free
           mbar_arrive_expect_tx(&full[i], kStageBytes);
-          load_b<FP8>(a, tmB, smB + i * kBBytes, smSF + i * C::kSfBytes, &full[i], t.nt, t.kb0 + i, kbt, pol_w);
+          load_b<FP8>(a, tmB, smB + i * kBBytes, smSF + i * C::kSfBytes, &full[i], nt, kf + i, kbt, pol_w);
         }
       }
       grid_dependency_wait();     // the gathered rows are written by the gather kernel
-      while (have && ok) {
-        Unit nx;
-        const bool more = FUSED ? false : unit_at<FUSED>(a, u + gridDim.x, kbt, nx);
+      while (u < a.units && ok) {
         // the kernel queued after this one (the gate) may start arriving once
         // every CTA has begun its last unit
-        if (!FUSED && !more) grid_launch_dependents();
-        const int mt = t.mt, nt = t.nt, kb0 = t.kb0, kbn = t.kbn;
+        if (!FUSED && u + gridDim.x >= a.units) grid_launch_dependents();
+        int mt, nt, sp, kb0, kbn;
+        unit_coords<FUSED>(a, u, mt, nt, sp);
+        unit_kb(a, u, sp, kb0, kbn);
         for (int kb = 0; kb < kbn; ++kb) {
           uint8_t* sf = smSF + stage * C::kSfBytes;
           if (u == first && kb < pre) {
@@ -819,11 +733,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if constexpr (FUSED) {
           u = atomicAdd(a.tickets, 1u);
           if (!publish(u < a.units ? u : -1)) ok = false;
-          have = unit_at<FUSED>(a, u, kbt, t);
         } else {
           u += gridDim.x;
-          have = more;
-          t = nx;
         }
       }
       if (!ok) {
@@ -858,12 +769,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             rphase ^= 1u;
           }
           if (u < 0) break;
-        }
-        Unit t;
-        if (!unit_at<FUSED>(a, u, kbt, t)) break;
-        if constexpr (!FUSED) {
-          Unit nx;
-          if (!unit_at<FUSED>(a, u + gridDim.x, kbt, nx)) grid_launch_dependents();
+        } else {
+          if (u >= a.units) break;
+          if (u + gridDim.x >= a.units) grid_launch_dependents();
         }
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
@@ -871,7 +779,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        const int kbn = t.kbn;
+        int kb_first, kbn;
+        unit_kb(a, u, remainder_unit(a, u) ? static_cast<int>((u - a.full_units) % a.rem_splits)
+                                           : static_cast<int>(u % a.splits),
+                kb_first, kbn);
         for (int kb = 0; kb < kbn; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
@@ -943,14 +854,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           rphase ^= 1u;
         }
         if (u < 0) break;
+      } else {
+        if (u >= a.units) break;
+        if (u + gridDim.x >= a.units) grid_launch_dependents();
       }
-      Unit t;
-      if (!unit_at<FUSED>(a, u, kbt, t)) break;
-      if constexpr (!FUSED) {
-        Unit nx;
-        if (!unit_at<FUSED>(a, u + gridDim.x, kbt, nx)) grid_launch_dependents();
-      }
-      const int mt = t.mt, nt = t.nt, sp = t.sp;
+      int mt, nt, sp;
+      unit_coords<FUSED>(a, u, mt, nt, sp);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         break;
@@ -960,25 +869,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       bool released = false;                         // the accumulator already handed back
       if constexpr (!FUSED) {
-        if (t.part >= 0) {
-          // stream-K: this part's fp32 sums to the workspace; the warp that
-          // completes the pair (per lane quarter) adds both parts into kv
-          const float* ws = a.sk_ws + (static_cast<int64_t>(t.bnd) * a.m_tiles + mt) * 2 * (kBM * kBN);
-          plain_epilogue<false>(a, t_row, m - lane, nt, 0, lane, smem_u32(epi),
-                                const_cast<float*>(ws) + (static_cast<int64_t>(t.part) * kBM + q * 32) * kBN, kBN);
-          __syncwarp();
-          __threadfence();
-          uint32_t old = 0;
-          if (lane == 0) old = atom_acq_rel_add_u32(a.sk_count + (t.bnd * a.m_tiles + mt) * 4 + q, 1u);
-          old = __shfl_sync(0xFFFFFFFFu, old, 0);
-          if (old == 1u && m - lane < a.M) {
-            __threadfence();
-            streamk_finish(a, ws, m - lane, q, nt, lane);
-          }
-        } else if (FP8 && a.out_mode == kOutBf16 && !t.rem) {
+        if (FP8 && a.out_mode == kOutBf16 && !remainder_unit(a, u)) {
           bf16_epilogue_release_first(a, t_row, m - lane, nt, lane, smem_u32(epi), &tempty[acc]);
           released = true;
-        } else if (t.rem) {
+        } else if (remainder_unit(a, u)) {
           // remainder unit j (tile j / rem_splits, K range sp): its fp32 sums go to
           // the workspace; launch_reduce_remainder adds the ranges up afterwards
           const int64_t j = u - a.full_units;

@@ -113,13 +113,6 @@ struct GemmArgs {
   int32_t rem_splits;
   int32_t rem_kb;
   float* rem_ws;         // [rem_tiles * rem_splits, 128, 256]
-  // Stream-K (splits == 1, bf16 kv, no remainder split): sk_groups groups of
-  // m_tiles CTAs share out the (N tile, K block) steps; a tile cut at a group
-  // boundary is computed in two parts whose fp32 sums meet in sk_ws, and the
-  // second part to finish (per lane quarter) writes kv = bf16(part 0 + part 1).
-  int32_t sk_groups;     // 0: off
-  float* sk_ws;          // [(sk_groups - 1) * m_tiles * 2, 128, 256]
-  uint32_t* sk_count;    // [(sk_groups - 1) * m_tiles * 4] parts finished; zeroed by the gather
   int32_t out_mode;      // GemmOut
   int32_t bulk_epilogue; // plain epilogue stores by per-row bulk copies (large batches)
   int32_t keep_weight;   // weight tiles L2 evict-last (shared by many M tiles) instead of evict-first
