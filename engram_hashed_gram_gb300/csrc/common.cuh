@@ -117,6 +117,12 @@ __device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* src, 
       : "memory");
 }
 
+// Asks the L2 to fetch `bytes` (16-byte aligned, a multiple of 16) at p; no
+// completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -860,6 +860,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       int mt, nt, sp;
       unit_coords<FUSED>(a, u, mt, nt, sp);
+      if constexpr (FUSED) {
+        // the rows of x this warp's epilogue of the unit will read, asked of
+        // the L2 now, while the unit's MMAs still run
+        const int64_t mr = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
+        if (mr < a.M) {
+          if (nt < a.key_n_tiles) {
+            const int s = nt * kBN / a.dim, d0 = nt * kBN - s * a.dim;
+            prefetch_l2(a.x + (mr * a.hc + s) * a.dim + d0, kBN * 2);
+          } else {
+            const int d0 = (nt - a.key_n_tiles) * kBN;
+            for (int s = 0; s < a.hc; ++s) prefetch_l2(a.x + (mr * a.hc + s) * a.dim + d0, kBN * 2);
+          }
+        }
+      }
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         break;
