@@ -23,6 +23,7 @@ struct engram_ctx {
   engram_weights w;
   int device;
   int num_sms;
+  int pair_slots;             // CTA pairs of the pair projection that fit at once (0: not used)
   int sm_budget;              // SMs the projection's persistent grid may occupy (engram_set_sm_budget)
   int32_t test_hooks;         // engram_test_hook bits
   int32_t K;
@@ -63,6 +64,7 @@ struct Plan {
   int64_t units;
   int32_t rem_tiles;    // tiles of the partial last wave cut into K ranges (0: none)
   int32_t rem_splits;
+  bool pair;            // CTA pairs (tcgen05 cta_group::2): units are 256 x 256 tiles
 };
 
 constexpr int kMaxRemSplits = 4;
@@ -90,6 +92,18 @@ bool wants_fused(const engram_ctx* c, int64_t M) {
   if (c->cfg.fuse_gate >= kFuseAlways) return true;
   return c->cfg.fuse_gate == kFuseAuto && M >= fuse_auto_min_tokens();
 }
+// Batches of at least this many tokens (bf16 weight, separate gate kernel)
+// are projected by CTA pairs (ENGRAM_PAIR_MIN overrides it for measurements;
+// 0 turns the pairs off).
+int64_t pair_min_tokens() {
+  static const int64_t v = [] {
+    const char* e = std::getenv("ENGRAM_PAIR_MIN");
+    const int64_t x = e != nullptr ? static_cast<int64_t>(std::atoll(e)) : int64_t{256};
+    return x <= 0 ? INT64_MAX : x;
+  }();
+  return v;
+}
+
 constexpr int64_t kBulkEpilogueTokens = 2048;
 constexpr int64_t kKeepWeightTokens = 2048;
 
@@ -131,6 +145,17 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
     best = forced;
   p.splits = best;
   p.units = tiles * best;
+  // CTA pairs: each SM holds and reads half of every weight tile it
+  // multiplies, so the shared memory's bandwidth, which bounds the one-CTA
+  // tile, goes further.  Whole tiles of 256 x 256, no remainder split.
+  if (best == 1 && !c->fp8 && !wants_fused(c, M) && M >= pair_min_tokens() && c->pair_slots > 0 &&
+      c->sm_budget == c->num_sms && !(forced >= 1 && forced <= kMaxSplits)) {
+    const int64_t pair_units = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+    p.pair = true;
+    p.units = pair_units;
+    p.ctas = static_cast<int32_t>(2 * (pair_units < c->pair_slots ? pair_units : c->pair_slots));
+    return p;
+  }
   // Without split-K, a last wave of rem < sms tiles would leave SMs idle for
   // a whole tile's K loop: cut those tiles into rem_splits K ranges when that
   // shortens the last wave (each range's fp32 sums go to a workspace; the last
@@ -248,6 +273,11 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* 
   a.m_tiles = p.m_tiles;
   a.n_tiles = p.n_tiles;
   a.group_m = p.m_tiles < 16 ? p.m_tiles : 16;
+  if (p.pair) {
+    const int32_t m_pairs = (p.m_tiles + 1) / 2;
+    a.pair = 1;
+    a.group_m = m_pairs < 8 ? m_pairs : 8;       // 8 pairs = the same 16 M tiles per group
+  }
   a.units = p.units;
   a.full_units = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.splits;
   if (rem) {
@@ -443,6 +473,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
     return ENGRAM_EUNSUPPORTED;
   }
   ctx->sm_budget = ctx->num_sms;
+  ctx->pair_slots = 0;
   const int64_t mt = c.max_tokens > 0 ? c.max_tokens : 1;
   ctx->part_tokens = mt < kSplitMaxTokens ? mt : kSplitMaxTokens;
   const size_t hcd = static_cast<size_t>(c.hc_mult) * c.dim;
@@ -483,6 +514,7 @@ engram_status engram_create(engram_ctx** out, const engram_config* cfg, const en
     free_ctx(ctx);
     return ENGRAM_ECUDA;
   }
+  ctx->pair_slots = gemm_pair_slots(ctx->num_sms);
   if (!fp8 && !make_tmap_bf16(&ctx->tmW, w->wkv, static_cast<uint64_t>(N), static_cast<uint64_t>(K), kBN)) {
     free_ctx(ctx);
     return ENGRAM_ECUDA;

@@ -934,6 +934,251 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair projection
+// The projection for bf16 kv without split-K on pairs of CTAs (clusters of
+// two, neighbouring SMs) with tcgen05.mma.cta_group::2:
+//  * a unit is a 256 x 256 output tile -- two M tiles by one N tile -- over
+//    the whole K;
+//  * CTA r of the pair loads rows r*128 .. r*128+127 of the unit's A rows and
+//    rows r*128 .. of its weight tile (the first or the second 16 KB of the
+//    packed 32 KB tile) into its own shared memory, so each SM keeps and
+//    reads half the weight bytes per FLOP of the one-CTA kernel (the MMA
+//    takes the other half from the peer);
+//  * both CTAs' tensor copies count their bytes on the even CTA's stage
+//    barrier (the cta_group::2 form of the copy), so the even CTA's MMA thread
+//    issues the pair's MMAs as soon as a stage has landed in both, and each of
+//    its commits arrives on the barriers of both CTAs at once;
+//  * each CTA's epilogue drains its own tensor memory (its 128 rows) like the
+//    one-CTA kernel and reports the accumulator free to the even CTA.
+// Every wait is bounded, as in wkv_gemm_kernel.
+constexpr int kPairStages = 6;
+struct PairCfg {
+  static constexpr int kABytes = kBM * kBK * 2;                  // 16 KB: 128 rows of A
+  static constexpr int kBHalf = kBBytes / 2;                     // 16 KB: 128 rows of the weight tile
+  static constexpr int kStageBytes = kABytes + kBHalf;
+  static constexpr int kBarOffset = kPairStages * kStageBytes;
+  static constexpr int kNumBars = 2 * kPairStages + 2 + 2 + 1;   // full, empty, tfull, tempty, drain
+  static constexpr int kEpiOffset = kBarOffset + 256;
+  static constexpr size_t kSmemBytes = 1024 + kEpiOffset + 4 * kPlainWarpBytes;
+  static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+// Pair unit u -> (M pair p: M tiles 2p, 2p+1; N tile nt), rasterised in
+// groups of group_m M pairs, M fastest inside a group.
+__device__ __forceinline__ void pair_coords(const GemmArgs& a, int64_t u, int& mp, int& nt) {
+  const int m_pairs = (a.m_tiles + 1) >> 1;
+  const int64_t group_units = static_cast<int64_t>(a.group_m) * a.n_tiles;
+  const int64_t g = u / group_units;
+  const int64_t r = u - g * group_units;
+  const int gm0 = static_cast<int>(g) * a.group_m;
+  const int gm = min(a.group_m, m_pairs - gm0);
+  nt = static_cast<int>(r / gm);
+  mp = gm0 + static_cast<int>(r % gm);
+}
+
+template <bool BULK>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    wkv_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                         const GemmArgs a) {
+  using C = PairCfg;
+  constexpr int S = kPairStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;                             // stage s at s * kABytes
+  uint8_t* smB = smem + S * C::kABytes;            // stage s at s * kBHalf
+  const int kbt = a.K / kBK;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* full = bars;                           // even CTA: the stage landed in both CTAs
+  uint64_t* empty = bars + S;                      // the pair's MMAs are done with the stage
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = tfull + 2;                    // even CTA: 8 epilogue warps of the pair
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t pair = blockIdx.x >> 1;
+  const int64_t npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_arrive();                                // both CTAs' barriers exist before any copy counts on them
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_w = a.keep_weight ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t full_even[S];                       // the even CTA's stage barriers
+      for (int i = 0; i < S; ++i) full_even[i] = mapa_shared(&full[i], 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[S] = {};
+      bool ok = true;
+      int pre = 0;
+      if (pair < a.units) {                        // the weight halves of the first stages, before the wait
+        int mp, nt;
+        pair_coords(a, pair, mp, nt);
+        pre = min(S, kbt);
+        for (int i = 0; i < pre; ++i) {
+          if (rank == 0) mbar_arrive_expect_tx(&full[i], 2 * C::kStageBytes);
+          tma_load_2d_pair(smB + i * C::kBHalf, &tmW, full_even[i], 0,
+                           (nt * kbt + i) * kBN + static_cast<int32_t>(rank) * kBM, pol_w);
+        }
+      }
+      grid_dependency_wait();                      // the gathered rows are written by the gather kernel
+      for (int64_t u = pair; u < a.units && ok; u += npairs) {
+        if (u + npairs >= a.units) grid_launch_dependents();
+        int mp, nt;
+        pair_coords(a, u, mp, nt);
+        const int32_t row0 = mp * (2 * kBM) + static_cast<int32_t>(rank) * kBM;
+        for (int kb = 0; kb < kbt; ++kb) {
+          if (!(u == pair && kb < pre)) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+            tma_load_2d_pair(smB + stage * C::kBHalf, &tmW, full_even[stage], 0,
+                             (nt * kbt + kb) * kBN + static_cast<int32_t>(rank) * kBM, pol_w);
+          }
+          tma_load_2d_pair(smA + stage * C::kABytes, &tmA, full_even[stage], kb * kBK, row0, pol_a);
+          ++issued[stage];
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        raise_abort(abort_flag, a.err);
+        // the even CTA waits for the copies in flight (they count on its barriers)
+        if (rank == 0)
+          for (int i = 0; i < S; ++i)
+            if (issued[i] > 0) mbar_wait(&full[i], (issued[i] - 1u) & 1u, nullptr, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  }
+  else if (warp == 1) {
+    grid_dependency_wait();
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      const uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t u = pair; u < a.units && ok; u += npairs) {
+        if (u + npairs >= a.units) grid_launch_dependents();
+        if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < kbt; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smA + stage * C::kABytes));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smB + stage * C::kBHalf));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit_pair(&empty[stage], 3);      // the stage is free in both CTAs
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[acc], 3);          // the accumulator is ready in both CTAs
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued completes before either CTA frees its tensor memory
+      umma_commit_pair(drain, 1);
+      mbar_wait(drain, 0, nullptr, kDrainLimitNs);
+      if (!ok) raise_abort(abort_flag, a.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    grid_dependency_wait();
+    const int q = warp & 3;
+    uint8_t* epi = smem + C::kEpiOffset + (warp - 2) * kPlainWarpBytes;
+    const uint32_t tempty_even[2] = {mapa_shared(&tempty[0], 0), mapa_shared(&tempty[1], 0)};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int64_t u = pair; u < a.units; u += npairs) {
+      if (u + npairs >= a.units) grid_launch_dependents();
+      int mp, nt;
+      pair_coords(a, u, mp, nt);
+      if (!mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int64_t m0 = static_cast<int64_t>(mp) * (2 * kBM) + static_cast<int64_t>(rank) * kBM + q * 32;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      plain_epilogue<BULK>(a, t_row, m0, nt, 0, lane, smem_u32(epi));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_remote(tempty_even[acc]);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) raise_abort(abort_flag, a.err);
+    __syncwarp();
+  }
+
+  // neither CTA frees its tensor memory before the pair's MMAs and both
+  // epilogues are done
+  tc_fence_before();
+  __syncthreads();
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
 template <int A_ROWS, int STAGES>
 cudaError_t set_smem_attr() {
   using C = Cfg<A_ROWS, STAGES>;
@@ -1096,7 +1341,33 @@ cudaError_t gemm_prepare() {
   cudaError_t e = set_smem_attr<128, 4>();
   if (e == cudaSuccess) e = set_smem_attr<64, 5>();
   if (e == cudaSuccess) e = set_smem_attr<32, 5>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(wkv_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(PairCfg::kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(wkv_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(PairCfg::kSmemBytes));
   return e;
+}
+
+int gemm_pair_slots(int num_sms) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, wkv_gemm_pair_kernel<false>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters < num_sms / 2 ? clusters : num_sms / 2;
 }
 
 cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* packed, cudaStream_t stream) {
@@ -1127,6 +1398,29 @@ cudaError_t launch_pack_sfb(const uint8_t* wkv_scale, int64_t N, int64_t K, uint
 cudaError_t launch_gemm(const void* rows, const CUtensorMap& tmB, const GemmArgs& a, int ctas,
                         cudaStream_t stream) {
   if (a.units == 0) return cudaSuccess;
+  if (a.pair) {                                     // CTA pairs: 128-row A boxes, grid of whole clusters
+    // the packed weight as 128-byte rows (each 32 KB tile is 256 of them, already
+    // in the swizzled order): a box of 128 rows is one CTA's half of a tile
+    CUtensorMap tmA, tmW;
+    auto enc = encode_fn();
+    const uint64_t w_rows = static_cast<uint64_t>(a.N) * static_cast<uint64_t>(a.K / kBK);
+    const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(kBK), w_rows};
+    const cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(kBK * 2)};
+    const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (a.fp8 || a.out_mode != kOutBf16 || a.wpack == nullptr || (ctas & 1) != 0 || enc == nullptr ||
+        !make_tmap_bf16(&tmA, rows, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), kBM) ||
+        enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(a.wpack), wdims, wstrides, wbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(ctas));
+    if (a.bulk_epilogue)
+      return launch_pdl(wkv_gemm_pair_kernel<true>, grid, dim3(kGemmThreads), PairCfg::kSmemBytes, stream, 2, tmA,
+                        tmW, a);
+    return launch_pdl(wkv_gemm_pair_kernel<false>, grid, dim3(kGemmThreads), PairCfg::kSmemBytes, stream, 2, tmA,
+                      tmW, a);
+  }
   const int ar = gemm_a_rows(a.M);
   CUtensorMap tmA;
   const bool mapped =

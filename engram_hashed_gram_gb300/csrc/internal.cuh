@@ -113,6 +113,8 @@ struct GemmArgs {
   int32_t rem_splits;
   int32_t rem_kb;
   float* rem_ws;         // [rem_tiles * rem_splits, 128, 256]
+  int32_t pair;          // CTA pairs (tcgen05 cta_group::2): units are 256 x 256 tiles, group_m counts M
+                         // pairs; bf16 kv, whole K, launched in clusters of two
   int32_t out_mode;      // GemmOut
   int32_t bulk_epilogue; // plain epilogue stores by per-row bulk copies (large batches)
   int32_t keep_weight;   // weight tiles L2 evict-last (shared by many M tiles) instead of evict-first
@@ -141,6 +143,8 @@ struct GemmArgs {
   float inv_sqrt_dim;
 };
 cudaError_t gemm_prepare();   // per-device one-time kernel attributes
+// How many CTA pairs of the pair projection fit on the device at once (0: none).
+int gemm_pair_slots(int num_sms);
 // Rows of the A (gathered rows) box the projection uses for a batch of M tokens.
 int gemm_a_rows(int64_t M);
 // Whether the projection variant for M tokens has shared memory for the fused epilogue.

@@ -1,8 +1,8 @@
 """GPU parity of the CUDA path against the oracle, through the C ABI, on the
 tiny table (24 prime ranges above 4096, 100,776 rows): shapes that span one
 and several 128-token tiles with ragged tails, the whole-K decode plan, the
-split-K plan (under an SM budget) and the single-pass prefill plan, masks,
-in-place calls, out-of-range ids and argument errors."""
+split-K plan (under an SM budget), the single-pass plans on one CTA and on
+CTA pairs, masks, in-place calls, out-of-range ids and argument errors."""
 import dataclasses
 
 import numpy as np
@@ -318,9 +318,10 @@ def test_split_k_plans(tiny, budget):
 
 
 def test_remainder_split_tiles(tiny):
-    """1,300 tokens make 11 x 100 = 1,100 output tiles: seven full waves of 152
-    and 36 tiles left over, which the plan cuts into four K ranges each (their
-    fp32 sums reduced in range order by a separate kernel).  Those tiles hold
+    """1,300 tokens make 11 x 100 = 1,100 output tiles: with the projection
+    held to 137 SMs (so that the one-CTA kernel runs), eight full waves and 4
+    tiles left over, which the plan cuts into four K ranges each (their fp32
+    sums reduced in range order by a separate kernel).  Those tiles hold
     the value columns of every token; every token is checked against the
     oracle, and forward equals lookup_project + gate_apply bit for bit."""
     from engram_hashed_gram_gb300.layer import EngramLayer
@@ -334,11 +335,20 @@ def test_remainder_split_tiles(tiny):
         gates = torch.empty((2, 650, 4), dtype=torch.float32, device="cuda")
         split = layer.gate_apply(kv, x, mask, gates=gates)
         assert layer.sync_status()[0] == 0
+        # on all SMs this batch takes CTA pairs (whole 256 x 256 tiles); on 137
+        # SMs the one-CTA plan cuts the 4 tiles of its last wave into K ranges
         assert layer.plan(1300) == (1, 152)
-        # gather, projection, the remainder's sums, gate; no remainder at 1,216 tokens (8 full waves)
+        assert layer.forward_kernels(1300) == 3
+        layer.set_sm_budget(137)
+        assert layer.plan(1300) == (1, 137)
+        # gather, projection, the remainder's sums, gate; no remainder at 1,233 tokens (9 full waves)
         assert layer.forward_kernels(1300) == 4
-        assert layer.forward_kernels(1216) == 3
+        assert layer.forward_kernels(1233) == 3
         assert layer.forward_kernels(64) == 3 and layer.forward_kernels(0) == 0
+        out = layer.forward(ids, x, mask)
+        kv = layer.lookup_project(ids)
+        split = layer.gate_apply(kv, x, mask, gates=gates)
+        assert layer.sync_status()[0] == 0
         assert torch.equal(out.view(torch.int16), split.view(torch.int16))
         M = 1300
         summary = P.check_layer(w, inp, np.arange(M), SD.device_bits(out.reshape(M, 4, -1)),
@@ -347,3 +357,37 @@ def test_remainder_split_tiles(tiny):
         print(summary)
     finally:
         layer.close()
+
+
+@pytest.mark.parametrize("B,T", [(1, 256), (3, 100), (1, 1000)])
+def test_cta_pair_projection(tiny, B, T):
+    """From 256 tokens on, the projection runs on CTA pairs (tcgen05
+    cta_group::2, 256 x 256 tiles; 300 tokens leave the odd CTA of the last
+    pair without a row of the batch).  Held to 150 SMs the same batch takes
+    the one-CTA kernel: both are checked against the oracle on every token,
+    and their kv agree within the dot-product bound."""
+    w, inp = _inputs(tiny, B, T, mask_frac=0.1, seed=12)
+    ids, x, mask = _dev(inp)
+    layer = tiny["layer"]
+    M = B * T
+    res = {}
+    try:
+        for budget in (0, 150):
+            layer.set_sm_budget(budget)
+            out = layer.forward(ids, x, mask)
+            kv = layer.lookup_project(ids)
+            gates = torch.empty((B, T, 4), dtype=torch.float32, device="cuda")
+            split = layer.gate_apply(kv, x, mask, gates=gates)
+            assert layer.sync_status()[0] == 0
+            assert torch.equal(out.view(torch.int16), split.view(torch.int16))
+            P.check_layer(w, inp, np.arange(M), SD.device_bits(out), gates.cpu().numpy(), SD.device_bits(kv),
+                          f"budget {budget}")
+            res[budget] = SD.device_bits(kv).reshape(M, -1)
+    finally:
+        layer.set_sm_budget(0)
+    assert layer.plan(M) == (1, 152)
+    rows = P.oracle_rows(w, inp, np.arange(M))
+    bound = P.kv_bound(rows, P.weight_values(inp), res[150], w.K)
+    diff = np.abs(O.bf16_value(res[0]) - O.bf16_value(res[150]))
+    assert np.all(diff <= 2 * bound)
+    print(f"{M} tokens: pair vs one-CTA kv identical in {float((diff == 0).mean()):.6f} of the elements")
