@@ -150,10 +150,29 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
   // tile, goes further.  Whole tiles of 256 x 256, no remainder split.
   if (best == 1 && !c->fp8 && !wants_fused(c, M) && M >= pair_min_tokens() && c->pair_slots > 0 &&
       c->sm_budget == c->num_sms && !(forced >= 1 && forced <= kMaxSplits)) {
-    const int64_t pair_units = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+    const int64_t pair_tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+    const int64_t slots = c->pair_slots;
     p.pair = true;
-    p.units = pair_units;
-    p.ctas = static_cast<int32_t>(2 * (pair_units < c->pair_slots ? pair_units : c->pair_slots));
+    p.units = pair_tiles;
+    // a small last wave of pair tiles is cut into K ranges, as for one-CTA
+    // tiles below (4,096 tokens: 1,600 tiles on 76 pairs leave 4)
+    const int64_t prem = pair_tiles % slots;
+    if (c->rem_ws != nullptr && pair_tiles > slots && prem > 0 && prem <= slots / 4) {
+      int64_t best_rem = kbt;
+      for (int32_t sp = 2; sp <= kMaxRemSplits; ++sp) {
+        if (kbt % sp != 0) continue;
+        const int64_t cost = ((prem * sp + slots - 1) / slots) * (kbt / sp);
+        if (cost < best_rem) {
+          best_rem = cost;
+          p.rem_splits = sp;
+        }
+      }
+      if (p.rem_splits > 0) {
+        p.rem_tiles = static_cast<int32_t>(prem);
+        p.units = (pair_tiles - prem) + prem * p.rem_splits;
+      }
+    }
+    p.ctas = static_cast<int32_t>(2 * (p.units < slots ? p.units : slots));
     return p;
   }
   // Without split-K, a last wave of rem < sms tiles would leave SMs idle for
@@ -281,7 +300,7 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* 
   a.units = p.units;
   a.full_units = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.splits;
   if (rem) {
-    a.full_units = static_cast<int64_t>(p.m_tiles) * p.n_tiles - p.rem_tiles;
+    a.full_units = (p.pair ? static_cast<int64_t>((p.m_tiles + 1) / 2) : p.m_tiles) * p.n_tiles - p.rem_tiles;
     a.rem_tiles = p.rem_tiles;
     a.rem_splits = p.rem_splits;
     a.rem_kb = (c->K / (c->fp8 ? 128 : kBK)) / p.rem_splits;

@@ -977,6 +977,25 @@ __device__ __forceinline__ void pair_coords(const GemmArgs& a, int64_t u, int& m
   mp = gm0 + static_cast<int>(r % gm);
 }
 
+// Pair unit u: its tile (mp, nt) and K blocks [kb0, kb0 + kbn).  Units past
+// full_units are the remainder: the last rem_tiles pair tiles of the raster
+// order, each cut into rem_splits K ranges of rem_kb blocks (range j % rem_splits
+// of tile j / rem_splits); returns that j, or -1 for a whole tile.
+__device__ __forceinline__ int64_t pair_unit(const GemmArgs& a, int64_t u, int kbt, int& mp, int& nt, int& kb0,
+                                             int& kbn) {
+  if (a.rem_splits > 0 && u >= a.full_units) {
+    const int64_t j = u - a.full_units;
+    pair_coords(a, a.full_units + j / a.rem_splits, mp, nt);
+    kb0 = static_cast<int>(j % a.rem_splits) * a.rem_kb;
+    kbn = a.rem_kb;
+    return j;
+  }
+  pair_coords(a, u, mp, nt);
+  kb0 = 0;
+  kbn = kbt;
+  return -1;
+}
+
 template <bool BULK>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     wkv_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -1042,22 +1061,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       int pre = 0;
       if (pair < a.units) {                        // the weight halves of the first stages, before the wait
-        int mp, nt;
-        pair_coords(a, pair, mp, nt);
-        pre = min(S, kbt);
+        int mp, nt, kb0, kbn;
+        pair_unit(a, pair, kbt, mp, nt, kb0, kbn);
+        pre = min(S, kbn);
         for (int i = 0; i < pre; ++i) {
           if (rank == 0) mbar_arrive_expect_tx(&full[i], 2 * C::kStageBytes);
           tma_load_2d_pair(smB + i * C::kBHalf, &tmW, full_even[i], 0,
-                           (nt * kbt + i) * kBN + static_cast<int32_t>(rank) * kBM, pol_w);
+                           (nt * kbt + kb0 + i) * kBN + static_cast<int32_t>(rank) * kBM, pol_w);
         }
       }
       grid_dependency_wait();                      // the gathered rows are written by the gather kernel
       for (int64_t u = pair; u < a.units && ok; u += npairs) {
         if (u + npairs >= a.units) grid_launch_dependents();
-        int mp, nt;
-        pair_coords(a, u, mp, nt);
+        int mp, nt, kb0, kbn;
+        pair_unit(a, u, kbt, mp, nt, kb0, kbn);
         const int32_t row0 = mp * (2 * kBM) + static_cast<int32_t>(rank) * kBM;
-        for (int kb = 0; kb < kbt; ++kb) {
+        for (int kb = 0; kb < kbn; ++kb) {
           if (!(u == pair && kb < pre)) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
               ok = false;
@@ -1065,9 +1084,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
             tma_load_2d_pair(smB + stage * C::kBHalf, &tmW, full_even[stage], 0,
-                             (nt * kbt + kb) * kBN + static_cast<int32_t>(rank) * kBM, pol_w);
+                             (nt * kbt + kb0 + kb) * kBN + static_cast<int32_t>(rank) * kBM, pol_w);
           }
-          tma_load_2d_pair(smA + stage * C::kABytes, &tmA, full_even[stage], kb * kBK, row0, pol_a);
+          tma_load_2d_pair(smA + stage * C::kABytes, &tmA, full_even[stage], (kb0 + kb) * kBK, row0, pol_a);
           ++issued[stage];
           if (++stage == S) {
             stage = 0;
@@ -1103,7 +1122,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < kbt; ++kb) {
+        int mp, nt, kb0, kbn;
+        pair_unit(a, u, kbt, mp, nt, kb0, kbn);
+        for (int kb = 0; kb < kbn; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -1144,8 +1165,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     for (int64_t u = pair; u < a.units; u += npairs) {
       if (u + npairs >= a.units) grid_launch_dependents();
-      int mp, nt;
-      pair_coords(a, u, mp, nt);
+      int mp, nt, kb0, kbn;
+      const int64_t j = pair_unit(a, u, kbt, mp, nt, kb0, kbn);
       if (!mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         break;
@@ -1153,7 +1174,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int64_t m0 = static_cast<int64_t>(mp) * (2 * kBM) + static_cast<int64_t>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      plain_epilogue<BULK>(a, t_row, m0, nt, 0, lane, smem_u32(epi));
+      if (j >= 0) {
+        // remainder range j % rem_splits of tile j / rem_splits: this CTA's
+        // 128 rows of fp32 sums to the workspace, [tile][range][CTA][128][256]
+        float* ws = a.rem_ws + ((j * 2 + rank) * kBM + q * 32) * kBN;
+        plain_epilogue<false>(a, t_row, m0, nt, 0, lane, smem_u32(epi), ws, kBN);
+      } else {
+        plain_epilogue<BULK>(a, t_row, m0, nt, 0, lane, smem_u32(epi));
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -1265,19 +1293,27 @@ __global__ void __launch_bounds__(256) pack_sfb_kernel(const uint8_t* __restrict
 __global__ void __launch_bounds__(256) reduce_remainder_kernel(const GemmArgs a) {
   grid_dependency_wait();        // the projection wrote the ranges' sums
   grid_launch_dependents();
-  const int64_t total = static_cast<int64_t>(a.rem_tiles) * kBM * 32;
-  const int64_t tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
-  const int64_t range_stride = static_cast<int64_t>(kBM) * kBN;
+  // one-CTA tiles: workspace [tile][range][128][256]; CTA pairs: 256-row
+  // tiles, [tile][range][CTA][128][256] (range r of a tile is 2 * 128 rows on)
+  const int tile_rows = a.pair ? 2 * kBM : kBM;
+  const int64_t total = static_cast<int64_t>(a.rem_tiles) * tile_rows * 32;
+  const int64_t range_stride = static_cast<int64_t>(tile_rows) * kBN;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int lane = static_cast<int>(i & 31);
-    const int row = static_cast<int>((i >> 5) % kBM);
-    const int64_t tr = (i >> 5) / kBM;
+    const int row = static_cast<int>((i >> 5) % tile_rows);
+    const int64_t tr = (i >> 5) / tile_rows;
     int mt, nt;
-    raster(a, tiles - a.rem_tiles + tr, a.n_tiles, mt, nt);
-    const int64_t m = static_cast<int64_t>(mt) * kBM + row;
+    int64_t m;
+    if (a.pair) {
+      pair_coords(a, a.full_units + tr, mt, nt);
+      m = static_cast<int64_t>(mt) * (2 * kBM) + row;
+    } else {
+      raster(a, static_cast<int64_t>(a.m_tiles) * a.n_tiles - a.rem_tiles + tr, a.n_tiles, mt, nt);
+      m = static_cast<int64_t>(mt) * kBM + row;
+    }
     if (m >= a.M) continue;
-    const float* p = a.rem_ws + (tr * a.rem_splits * kBM + row) * kBN + lane * 8;
+    const float* p = a.rem_ws + (tr * a.rem_splits * tile_rows + row) * kBN + lane * 8;
     float4 lo = __ldcg(reinterpret_cast<const float4*>(p)), hi = __ldcg(reinterpret_cast<const float4*>(p) + 1);
     for (int s = 1; s < a.rem_splits; ++s) {
       const float4* ps = reinterpret_cast<const float4*>(p + s * range_stride);
@@ -1381,7 +1417,7 @@ cudaError_t launch_pack_wkv(const uint16_t* wkv, int64_t N, int64_t K, uint8_t* 
 
 cudaError_t launch_reduce_remainder(const GemmArgs& a, int num_sms, cudaStream_t stream) {
   if (a.rem_splits == 0 || a.rem_tiles == 0) return cudaSuccess;
-  const int64_t total = static_cast<int64_t>(a.rem_tiles) * kBM * 32;
+  const int64_t total = static_cast<int64_t>(a.rem_tiles) * (a.pair ? 2 * kBM : kBM) * 32;
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(num_sms) * 8);
   return launch_pdl(reduce_remainder_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1, a);
 }

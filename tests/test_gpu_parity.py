@@ -359,17 +359,22 @@ def test_remainder_split_tiles(tiny):
         layer.close()
 
 
-@pytest.mark.parametrize("B,T", [(1, 256), (3, 100), (1, 1000)])
+@pytest.mark.parametrize("B,T", [(1, 256), (3, 100), (1, 1000), (1, 1750)])
 def test_cta_pair_projection(tiny, B, T):
     """From 256 tokens on, the projection runs on CTA pairs (tcgen05
     cta_group::2, 256 x 256 tiles; 300 tokens leave the odd CTA of the last
-    pair without a row of the batch).  Held to 150 SMs the same batch takes
-    the one-CTA kernel: both are checked against the oracle on every token,
-    and their kv agree within the dot-product bound."""
+    pair without a row of the batch; 1,750 tokens make 700 pair tiles, 16 more
+    than 9 waves of 76 pairs, which the plan cuts into K ranges).  Held to 150
+    SMs the same batch takes the one-CTA kernel: both are checked against the
+    oracle on every token, and their kv agree within the dot-product bound."""
+    from engram_hashed_gram_gb300.layer import EngramLayer
     w, inp = _inputs(tiny, B, T, mask_frac=0.1, seed=12)
     ids, x, mask = _dev(inp)
-    layer = tiny["layer"]
+    dev = tiny["dev"]
+    layer = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=2048)
     M = B * T
+    if M == 1750:
+        assert layer.forward_kernels(M) == 4           # gather, pairs, the remainder's sums, gate
     res = {}
     try:
         for budget in (0, 150):
@@ -383,9 +388,10 @@ def test_cta_pair_projection(tiny, B, T):
             P.check_layer(w, inp, np.arange(M), SD.device_bits(out), gates.cpu().numpy(), SD.device_bits(kv),
                           f"budget {budget}")
             res[budget] = SD.device_bits(kv).reshape(M, -1)
-    finally:
         layer.set_sm_budget(0)
-    assert layer.plan(M) == (1, 152)
+        assert layer.plan(M) == (1, 152)
+    finally:
+        layer.close()
     rows = P.oracle_rows(w, inp, np.arange(M))
     bound = P.kv_bound(rows, P.weight_values(inp), res[150], w.K)
     diff = np.abs(O.bf16_value(res[0]) - O.bf16_value(res[150]))
