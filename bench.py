@@ -148,10 +148,21 @@ GEMM_SOURCES = ["engram_hashed_gram_gb300/csrc/gemm.cu", "engram_hashed_gram_gb3
                 "engram_hashed_gram_gb300/csrc/internal.cuh"]
 
 
+def plan_key(info):
+    """The plan as the traffic record names it: <split-K factor>x<CTAs>, with
+    a trailing p for CTA pairs and r<tiles>x<ranges> for a remainder split."""
+    key = "%dx%d" % (info["splits"], info["ctas"])
+    if info.get("cta_pairs"):
+        key += "p"
+    if info.get("rem_tiles"):
+        key += "r%dx%d" % (info["rem_tiles"], info["rem_splits"])
+    return key
+
+
 def recorded_traffic(workload, plan=None):
     """DRAM bytes per launch of the projection kernel from the committed ncu
     summary, if it was taken on the current kernel source (and, when the record
-    names one, the same plan: split-K factor x CTAs); else None."""
+    names one, the same plan, plan_key); else None."""
     p = os.path.join(ROOT, "profiles", "wkv_gemm_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -159,7 +170,7 @@ def recorded_traffic(workload, plan=None):
     for line in open(p):
         kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
         if kv.get("workload") == workload and kv.get("source_sha256") == digest:
-            if plan is not None and "plan" in kv and kv["plan"] != "%dx%d" % tuple(plan):
+            if plan is not None and "plan" in kv and kv["plan"] != plan:
                 continue
             return float(kv["dram_bytes_per_launch"])
     return None
@@ -461,6 +472,7 @@ def run_ours(args, w, rank, world, local_rank):
         pk = dict(pk, bf16_tflops=2.0 * pk["bf16_tflops"], bf16_tflops_sustained=None if sus is None else 2.0 * sus,
                   source=pk["source"] + " bf16 x 2 (nominal fp8/bf16)")
     splits, ctas = layer.plan(M)
+    plan_info = layer.describe_plan(M)
     kernels_per_step = layer.forward_kernels(M)
     gather_ms = statistics.mean(s[0] for s in stages)
     proj_ms = statistics.mean(s[1] for s in stages)
@@ -478,8 +490,9 @@ def run_ours(args, w, rank, world, local_rank):
             # the peak a dense GEMM holds for seconds under the power cap
             roof["frac_of_sustained"] = roof["achieved"] / pk["bf16_tflops_sustained"]
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(w.name, (splits, ctas))
-    roof["kernel"] = "wkv_gemm_kernel (tcgen05 projection)"
+    roof["traffic"] = recorded_traffic(w.name, plan_key(plan_info))
+    roof["kernel"] = ("wkv_gemm_pair_kernel (tcgen05 cta_group::2 projection on CTA pairs)" if plan_info["cta_pairs"]
+                      else "wkv_gemm_kernel (tcgen05 projection)")
     roof["peak_source"] = pk["source"]
     roof["algorithmic_bytes_per_launch"] = pbytes
     roof["algorithmic_flops_per_launch"] = pflops
@@ -506,7 +519,7 @@ def run_ours(args, w, rank, world, local_rank):
                            "achieved_us": 1e3 * ms_per_step, "frac": t_roof / (ms_per_step * 1e-3)},
         "stages_ms": {"gather": gather_ms, "projection": proj_ms, "gate": gate_ms},
         "gather_gbs": gather_bytes(w, M) / (gather_ms * 1e-3) / 1e9,
-        "plan": {"splits": splits, "ctas": ctas},
+        "plan": plan_info,
         "clocks": clocks,
     }
     layer.close()

@@ -50,6 +50,17 @@ class EngramConfig(ctypes.Structure):
     ]
 
 
+class EngramPlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("splits", c_int32),
+        ("ctas", c_int32),
+        ("cta_pairs", c_int32),
+        ("rem_tiles", c_int32),
+        ("rem_splits", c_int32),
+        ("fused_gate", c_int32),
+    ]
+
+
 class EngramHashConfig(ctypes.Structure):
     _fields_ = [
         ("n_layers", c_int32),
@@ -87,6 +98,7 @@ ENGRAM_FUNCS = {
     "engram_sync_status": (c_int32, [c_void_p, c_void_p, POINTER(c_int64)]),
     "engram_plan": (c_int32, [c_void_p, c_int64, POINTER(c_int32), POINTER(c_int32)]),
     "engram_forward_kernels": (c_int32, [c_void_p, c_int64, POINTER(c_int32)]),
+    "engram_describe_plan": (c_int32, [c_void_p, c_int64, POINTER(EngramPlanInfo)]),
     "engram_set_sm_budget": (c_int32, [c_void_p, c_int32]),
     "engram_test_hook": (c_int32, [c_void_p, c_int32]),
     "engram_forward_noalloc": (c_int32, [POINTER(EngramConfig), POINTER(EngramWeights), c_void_p, c_void_p,

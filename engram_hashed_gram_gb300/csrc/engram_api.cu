@@ -435,7 +435,7 @@ const char* engram_status_string(engram_status s) {
   return "unknown status";
 }
 
-int32_t engram_abi_version(void) { return 103; }
+int32_t engram_abi_version(void) { return 104; }
 
 engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w) {
   if (out == nullptr || cfg == nullptr || w == nullptr) return ENGRAM_EINVAL;
@@ -675,6 +675,18 @@ engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, int32_t* spli
   const Plan p = make_plan(ctx, m_tokens);
   if (splits != nullptr) *splits = p.splits;
   if (ctas != nullptr) *ctas = p.ctas;
+  return ENGRAM_OK;
+}
+
+engram_status engram_describe_plan(const engram_ctx* ctx, int64_t m_tokens, engram_plan_info* info) {
+  if (ctx == nullptr || m_tokens < 0 || info == nullptr) return ENGRAM_EINVAL;
+  const Plan p = make_plan(ctx, m_tokens);
+  info->splits = p.splits;
+  info->ctas = p.ctas;
+  info->cta_pairs = p.pair ? 1 : 0;
+  info->rem_tiles = p.rem_tiles;
+  info->rem_splits = p.rem_splits;
+  info->fused_gate = m_tokens > 0 && fuses(ctx, p, m_tokens) ? 1 : 0;
   return ENGRAM_OK;
 }
 

@@ -193,6 +193,12 @@ class EngramLayer:
         check(self._lib.engram_plan(self._ctx, m_tokens, ctypes.byref(s), ctypes.byref(c)), "engram_plan")
         return s.value, c.value
 
+    def describe_plan(self, m_tokens):
+        """The projection's plan for m_tokens tokens as a dict (engram_describe_plan)."""
+        info = _lib.EngramPlanInfo()
+        check(self._lib.engram_describe_plan(self._ctx, m_tokens, ctypes.byref(info)), "engram_describe_plan")
+        return {f: getattr(info, f) for f, _ in info._fields_}
+
     def forward_kernels(self, m_tokens):
         """How many kernels one forward over m_tokens tokens launches."""
         k = ctypes.c_int32(0)

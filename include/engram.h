@@ -232,6 +232,19 @@ ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, in
  * this changes kv's summation order for those tiles, not its tolerance.
  * Contexts with max_tokens <= 128 or fuse_gate set keep whole tiles.) */
 
+/* The projection's whole plan for B*T = m_tokens on this context (queues
+ * nothing).  ENGRAM_EINVAL for a NULL context or pointer or a negative count. */
+typedef struct {
+  int32_t splits;       /* split-K factor (1: every tile over the whole K) */
+  int32_t ctas;         /* CTAs of the projection's persistent grid */
+  int32_t cta_pairs;    /* 1: tiles of 256 x 256 on pairs of CTAs (tcgen05 cta_group::2, clusters of two),
+                           0: tiles of 128 x 256 on single CTAs */
+  int32_t rem_tiles;    /* tiles of a partial last wave cut into K ranges (0: none) */
+  int32_t rem_splits;   /* the K ranges each of them is cut into */
+  int32_t fused_gate;   /* 1: engram_forward forms the gate in the projection's epilogue */
+} engram_plan_info;
+ENGRAM_API engram_status engram_describe_plan(const engram_ctx* ctx, int64_t m_tokens, engram_plan_info* info);
+
 /* Number of kernels one engram_forward over m_tokens tokens launches on this
  * context (gather, projection, the remainder sums when the plan has them, gate;
  * 2 with the fused gate epilogue; 0 for no tokens).  Queues nothing.

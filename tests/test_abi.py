@@ -70,6 +70,9 @@ int main(void) {
   printf("engram_weights %zu\n", sizeof(engram_weights));
   F(engram_weights, table); F(engram_weights, scale); F(engram_weights, wkv); F(engram_weights, q_weight);
   F(engram_weights, k_weight); F(engram_weights, wkv_scale);
+  printf("engram_plan_info %zu\n", sizeof(engram_plan_info));
+  F(engram_plan_info, splits); F(engram_plan_info, ctas); F(engram_plan_info, cta_pairs);
+  F(engram_plan_info, rem_tiles); F(engram_plan_info, rem_splits); F(engram_plan_info, fused_gate);
   printf("engram_hash_config %zu\n", sizeof(engram_hash_config));
   F(engram_hash_config, n_layers); F(engram_hash_config, max_ngram_size); F(engram_hash_config, n_heads);
   F(engram_hash_config, max_batch); F(engram_hash_config, max_len); F(engram_hash_config, vocab_size);
@@ -84,8 +87,9 @@ int main(void) {
     assert int(c["engram_config"]) == ctypes.sizeof(libs.EngramConfig)
     assert int(c["engram_weights"]) == ctypes.sizeof(libs.EngramWeights)
     assert int(c["engram_hash_config"]) == ctypes.sizeof(libs.EngramHashConfig)
+    assert int(c["engram_plan_info"]) == ctypes.sizeof(libs.EngramPlanInfo)
     names = {libs.EngramConfig: "engram_config", libs.EngramWeights: "engram_weights",
-             libs.EngramHashConfig: "engram_hash_config"}
+             libs.EngramHashConfig: "engram_hash_config", libs.EngramPlanInfo: "engram_plan_info"}
     for T, cname in names.items():
         for f, _ in T._fields_:
             assert int(c[f"{cname}.{f}"]) == getattr(T, f).offset, f
@@ -93,7 +97,7 @@ int main(void) {
 
 def test_host_only_entry_points(libs):
     lib = libs.engram()
-    assert lib.engram_abi_version() == 103
+    assert lib.engram_abi_version() == 104
     for code, text in ((0, b"ok"), (-1, b"invalid argument"), (-4, b"hash id outside the table"),
                        (-5, b"kernel wait timed out"), (-6, b"unsupported shape or format"), (7, b"unknown status")):
         assert lib.engram_status_string(code) == text
@@ -111,6 +115,7 @@ def test_host_only_entry_points(libs):
     assert lib.engram_forward_rows(None, None, None, None, None, 1, 1, None) == -1
     assert lib.engram_sync_status(None, None, None) == -1
     assert lib.engram_plan(None, 1, None, None) == -1
+    assert lib.engram_describe_plan(None, 1, None) == -1
     assert lib.engram_set_sm_budget(None, 8) == -1
     assert lib.engram_test_hook(None, 1) == -1
     assert lib.engram_enable_stage_timing(None, 1) == -1

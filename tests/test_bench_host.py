@@ -40,16 +40,22 @@ def test_recorded_traffic_matches_workload_digest_and_plan(tmp_path, monkeypatch
     (prof / "wkv_gemm_traffic.txt").write_text(
         "# comment line\n"
         f"workload=w1 kernel=k plan=1x100 source_sha256={digest} dram_bytes_per_launch=123 read=120 write=3\n"
+        f"workload=w4 kernel=k plan=1x152pr16x4 source_sha256={digest} dram_bytes_per_launch=7 read=5 write=2\n"
         f"workload=w2 kernel=k source_sha256=0000000000000000 dram_bytes_per_launch=456 read=450 write=6\n"
         f"workload=w3 kernel=k source_sha256={digest} dram_bytes_per_launch=789 read=780 write=9\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "source_digest", lambda files: digest)
-    assert bench.recorded_traffic("w1", (1, 100)) == 123.0
+    one = bench.plan_key(dict(splits=1, ctas=100, cta_pairs=0, rem_tiles=0, rem_splits=0))
+    assert one == "1x100"
+    assert bench.recorded_traffic("w1", one) == 123.0
     assert bench.recorded_traffic("w1") == 123.0                 # no plan given: the record stands
-    assert bench.recorded_traffic("w1", (3, 152)) is None        # captured with another plan
-    assert bench.recorded_traffic("w2", (1, 100)) is None        # captured on other source
-    assert bench.recorded_traffic("w3", (8, 152)) == 789.0       # the record names no plan
-    assert bench.recorded_traffic("absent", (1, 100)) is None
+    assert bench.recorded_traffic("w1", "3x152") is None          # captured with another plan
+    assert bench.recorded_traffic("w2", one) is None              # captured on other source
+    assert bench.recorded_traffic("w3", "8x152") == 789.0         # the record names no plan
+    assert bench.recorded_traffic("absent", one) is None
+    pairs = bench.plan_key(dict(splits=1, ctas=152, cta_pairs=1, rem_tiles=16, rem_splits=4))
+    assert pairs == "1x152pr16x4" and bench.recorded_traffic("w4", pairs) == 7.0
+    assert bench.recorded_traffic("w4", "1x152p") is None         # pairs without the remainder split
 
 
 def test_committed_traffic_records_add_up():
