@@ -98,11 +98,13 @@ def weight_bytes(w):
     return w.N * w.K * 2 if w.wkv_fmt == 0 else w.N * w.K + w.N * w.K // 32
 
 
-def projection_bytes(w, M):
+def projection_bytes(w, M, fused=False):
     """Algorithmic bytes of one projection launch: the weight once, the
-    gathered rows read once, kv written once in bf16."""
+    gathered rows read once, kv written once in bf16 -- or, with the gate in
+    the epilogue, x read once and the output written once instead of kv."""
     a_bytes = w.K * 2 if w.wkv_fmt == 0 else w.K + w.K // 32   # bf16 rows, or codes + scales
-    return weight_bytes(w) + M * a_bytes + M * w.N * 2
+    out_bytes = 2 * w.hc_mult * w.dim * 2 if fused else w.N * 2
+    return weight_bytes(w) + M * a_bytes + M * out_bytes
 
 
 def gather_bytes(w, M):
@@ -150,12 +152,15 @@ GEMM_SOURCES = ["engram_hashed_gram_gb300/csrc/gemm.cu", "engram_hashed_gram_gb3
 
 def plan_key(info):
     """The plan as the traffic record names it: <split-K factor>x<CTAs>, with
-    a trailing p for CTA pairs and r<tiles>x<ranges> for a remainder split."""
+    a trailing p for CTA pairs, r<tiles>x<ranges> for a remainder split and f
+    for the gate in the projection's epilogue."""
     key = "%dx%d" % (info["splits"], info["ctas"])
     if info.get("cta_pairs"):
         key += "p"
     if info.get("rem_tiles"):
         key += "r%dx%d" % (info["rem_tiles"], info["rem_splits"])
+    if info.get("fused_gate"):
+        key += "f"
     return key
 
 
@@ -370,14 +375,18 @@ def run_ours(args, w, rank, world, local_rank):
 
     # ---- per-kernel durations: the same steps again with an event between the
     # kernels (events between kernels also stop them from overlapping, so these
-    # are each kernel's own duration, and they are not used for `value`)
-    layer.enable_stage_timing(True)
+    # are each kernel's own duration, and they are not used for `value`).  Each
+    # timed step directly follows an untimed one, as in the timed region, so
+    # that the GPU does not idle (and change its clocks) just before it.
     stages = []
     for i in range(args.steps):
         flush()
         layer.forward(ids, x, mask, out=out)
+        flush()
+        layer.enable_stage_timing(True)
+        layer.forward(ids, x, mask, out=out)
         stages.append(layer.stage_times())       # waits for this step's last event
-    layer.enable_stage_timing(False)
+        layer.enable_stage_timing(False)
 
     # keep the GPU busy a little longer so the clock sampler sees the load
     t_end = time.perf_counter() + 1.0
@@ -477,7 +486,7 @@ def run_ours(args, w, rank, world, local_rank):
     gather_ms = statistics.mean(s[0] for s in stages)
     proj_ms = statistics.mean(s[1] for s in stages)
     gate_ms = statistics.mean(s[2] for s in stages)
-    pbytes = projection_bytes(w, M)
+    pbytes = projection_bytes(w, M, fused=bool(plan_info["fused_gate"]))
     pflops = 2.0 * w.N * w.K * M
     t_mem = pbytes / (pk["hbm_gbs"] * 1e9)
     t_tc = pflops / (pk["bf16_tflops"] * 1e12)
@@ -493,6 +502,8 @@ def run_ours(args, w, rank, world, local_rank):
     roof["traffic"] = recorded_traffic(w.name, plan_key(plan_info))
     roof["kernel"] = ("wkv_gemm_pair_kernel (tcgen05 cta_group::2 projection on CTA pairs)" if plan_info["cta_pairs"]
                       else "wkv_gemm_kernel (tcgen05 projection)")
+    if plan_info["fused_gate"]:
+        roof["kernel"] += ", gate and residual add in its epilogue"
     roof["peak_source"] = pk["source"]
     roof["algorithmic_bytes_per_launch"] = pbytes
     roof["algorithmic_flops_per_launch"] = pflops

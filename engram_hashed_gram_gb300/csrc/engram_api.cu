@@ -76,25 +76,22 @@ constexpr int32_t kFuseAlways = 1;
 
 // Batches of at least this many tokens take the fused gate epilogue when
 // fuse_gate is 0 (ENGRAM_FUSE_MIN overrides it for measurements).
+// The library's choice (fuse_gate 0) fuses the gate into the CTA-pair
+// projection's epilogue from this many tokens on (ENGRAM_FUSE_MIN overrides it
+// for measurements).  Measured on GB300, one forward, fused against the
+// separate gate kernel: 512 tokens 148 / 131 us, 768 184 / 174, 1,024 236 /
+// 241, 2,048 392 / 418, 4,096 742 / 796, 8,192 1,455 / 1,579.  Below that the
+// value tiles' wait for all key tiles of their rows is not hidden.
 int64_t fuse_auto_min_tokens() {
   static const int64_t v = [] {
     const char* e = std::getenv("ENGRAM_FUSE_MIN");
-    return e != nullptr ? static_cast<int64_t>(std::atoll(e)) : INT64_MAX;
+    return e != nullptr ? static_cast<int64_t>(std::atoll(e)) : int64_t{1024};
   }();
   return v;
 }
 
-// Whether engram_forward over M tokens forms the gate in the projection's
-// epilogue when the plan allows it (bf16 weight, whole-K tiles, shared memory
-// for the fused variant).
-bool wants_fused(const engram_ctx* c, int64_t M) {
-  if (c->fp8 || !gemm_can_fuse(M)) return false;
-  if (c->cfg.fuse_gate >= kFuseAlways) return true;
-  return c->cfg.fuse_gate == kFuseAuto && M >= fuse_auto_min_tokens();
-}
-// Batches of at least this many tokens (bf16 weight, separate gate kernel)
-// are projected by CTA pairs (ENGRAM_PAIR_MIN overrides it for measurements;
-// 0 turns the pairs off).
+// Batches of at least this many tokens (bf16 weight) are projected by CTA
+// pairs (ENGRAM_PAIR_MIN overrides it for measurements; 0 turns the pairs off).
 int64_t pair_min_tokens() {
   static const int64_t v = [] {
     const char* e = std::getenv("ENGRAM_PAIR_MIN");
@@ -102,6 +99,22 @@ int64_t pair_min_tokens() {
     return x <= 0 ? INT64_MAX : x;
   }();
   return v;
+}
+
+// Whether a batch of M tokens may take the CTA-pair projection: bf16 weight,
+// all SMs (no run-ahead budget), and pairs that fit on the device.
+bool pair_eligible(const engram_ctx* c, int64_t M) {
+  return !c->fp8 && M >= pair_min_tokens() && c->pair_slots > 0 && c->sm_budget == c->num_sms;
+}
+
+// Whether engram_forward over M tokens forms the gate in the projection's
+// epilogue when the plan allows it (bf16 weight, whole-K tiles, shared memory
+// for the fused variant).  The library's choice takes it only on CTA pairs
+// (the one-CTA fused epilogue does not beat the separate gate kernel).
+bool wants_fused(const engram_ctx* c, int64_t M) {
+  if (c->fp8 || !gemm_can_fuse(M)) return false;
+  if (c->cfg.fuse_gate >= kFuseAlways) return true;
+  return c->cfg.fuse_gate == kFuseAuto && M >= fuse_auto_min_tokens() && pair_eligible(c, M);
 }
 
 constexpr int64_t kBulkEpilogueTokens = 2048;
@@ -147,17 +160,17 @@ Plan make_plan(const engram_ctx* c, int64_t M) {
   p.units = tiles * best;
   // CTA pairs: each SM holds and reads half of every weight tile it
   // multiplies, so the shared memory's bandwidth, which bounds the one-CTA
-  // tile, goes further.  Whole tiles of 256 x 256, no remainder split.
-  if (best == 1 && !c->fp8 && !wants_fused(c, M) && M >= pair_min_tokens() && c->pair_slots > 0 &&
-      c->sm_budget == c->num_sms && !(forced >= 1 && forced <= kMaxSplits)) {
+  // tile, goes further.  Tiles of 256 x 256.
+  if (best == 1 && pair_eligible(c, M) && !(forced >= 1 && forced <= kMaxSplits)) {
     const int64_t pair_tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
     const int64_t slots = c->pair_slots;
     p.pair = true;
     p.units = pair_tiles;
     // a small last wave of pair tiles is cut into K ranges, as for one-CTA
-    // tiles below (4,096 tokens: 1,600 tiles on 76 pairs leave 4)
+    // tiles below (4,096 tokens: 1,600 tiles on 76 pairs leave 4); not with
+    // the fused gate epilogue, which takes whole tiles
     const int64_t prem = pair_tiles % slots;
-    if (c->rem_ws != nullptr && pair_tiles > slots && prem > 0 && prem <= slots / 4) {
+    if (c->rem_ws != nullptr && !wants_fused(c, M) && pair_tiles > slots && prem > 0 && prem <= slots / 4) {
       int64_t best_rem = kbt;
       for (int32_t sp = 2; sp <= kMaxRemSplits; ++sp) {
         if (kbt % sp != 0) continue;
@@ -305,8 +318,6 @@ engram_status run_projection(engram_ctx* c, const int64_t* ids, const uint16_t* 
     a.rem_splits = p.rem_splits;
     a.rem_kb = (c->K / (c->fp8 ? 128 : kBK)) / p.rem_splits;
     a.rem_ws = c->rem_ws;
-  } else if (fuse) {
-    a.units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   }
   a.out_mode = p.splits == 1 ? kOutBf16 : kOutPartial;
   a.kv = kv_out;

@@ -47,6 +47,7 @@
 // descriptor picks the scale byte).  The accumulator is single-buffered: the
 // scales take tensor-memory columns 256 and up.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -133,11 +134,12 @@ __device__ __forceinline__ bool remainder_unit(const GemmArgs& a, int64_t u) {
 // key tiles of its M tile, comes a whole group of key tiles after them (they
 // are long finished by then), and the value tiles' heavier epilogues (x and
 // out of every stream) are spread over the run instead of bunched at its end.
-// Every unit a value tile waits for has a smaller index.
-__device__ __forceinline__ void fused_coords(const GemmArgs& a, int64_t u, int& mt, int& nt) {
+// Every unit a value tile waits for has a smaller index.  m_count is the
+// number of M units: M tiles, or M pairs for the CTA-pair kernel.
+__device__ __forceinline__ void fused_coords(const GemmArgs& a, int64_t u, int m_count, int& mt, int& nt) {
   const int KT = a.key_n_tiles;
   const int VT = a.n_tiles - a.key_n_tiles;
-  const int G = (a.m_tiles + a.group_m - 1) / a.group_m;
+  const int G = (m_count + a.group_m - 1) / a.group_m;
   int64_t off = 0;
   for (int seg = 0; seg < 2 * G; ++seg) {
     int g;
@@ -151,7 +153,7 @@ __device__ __forceinline__ void fused_coords(const GemmArgs& a, int64_t u, int& 
     } else {
       g = (seg >> 1) - 1, key = false;
     }
-    const int gm = min(a.group_m, a.m_tiles - g * a.group_m);
+    const int gm = min(a.group_m, m_count - g * a.group_m);
     const int64_t size = static_cast<int64_t>(gm) * (key ? KT : VT);
     if (u < off + size) {
       const int64_t l = u - off;
@@ -176,7 +178,7 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int64_t u, int& m
   sp = static_cast<int>(u % a.splits);
   const int64_t t = u / a.splits;
   if constexpr (FUSED) {
-    fused_coords(a, t, mt, nt);
+    fused_coords(a, t, a.m_tiles, mt, nt);
     return;
   }
   raster(a, t, a.n_tiles, mt, nt);
@@ -951,17 +953,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 //  * each CTA's epilogue drains its own tensor memory (its 128 rows) like the
 //    one-CTA kernel and reports the accumulator free to the even CTA.
 // Every wait is bounded, as in wkv_gemm_kernel.
-constexpr int kPairStages = 6;
-struct PairCfg {
+// Shared memory of the pair kernel.  The fused mode keeps five operand stages
+// (six otherwise) to make room for each epilogue warp's x staging buffers.
+constexpr int kXBufs = 3;                       // x staging buffers per epilogue warp (fused)
+constexpr int kXBufBytes = 4096;                // one x chunk: 32 tokens x 64 channels of one stream
+template <bool FUSED>
+struct PairCfgT {
+  static constexpr int kStages = FUSED ? 5 : 6;
   static constexpr int kABytes = kBM * kBK * 2;                  // 16 KB: 128 rows of A
   static constexpr int kBHalf = kBBytes / 2;                     // 16 KB: 128 rows of the weight tile
   static constexpr int kStageBytes = kABytes + kBHalf;
-  static constexpr int kBarOffset = kPairStages * kStageBytes;
-  static constexpr int kNumBars = 2 * kPairStages + 2 + 2 + 1;   // full, empty, tfull, tempty, drain
+  static constexpr int kXOffset = kStages * kStageBytes;         // 1024-byte aligned
+  static constexpr int kBarOffset = kXOffset + (FUSED ? 4 * kXBufs * kXBufBytes : 0);
+  // full, empty, tfull, tempty, drain; fused: each epilogue warp's x buffers
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + (FUSED ? 4 * kXBufs : 0);
   static constexpr int kEpiOffset = kBarOffset + 256;
-  static constexpr size_t kSmemBytes = 1024 + kEpiOffset + 4 * kPlainWarpBytes;
+  // plain: the epilogue's staging tile; fused: a key tile's 256 weight products
+  static constexpr int kEpiWarp = FUSED ? 1024 : kPlainWarpBytes;
+  static constexpr size_t kRingOffset = kEpiOffset + 4 * kEpiWarp;   // fused: the CTA's unit queue
+  static constexpr size_t kSmemBytes = 1024 + kRingOffset + (FUSED ? kRingBytes : 0);
   static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+  static_assert(kXOffset % 1024 == 0 && kXBufBytes % 1024 == 0, "x buffers take the 128-byte swizzle");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+using PairCfg = PairCfgT<false>;
+using PairFusedCfg = PairCfgT<true>;
+
+// The tensor maps of the fused pair epilogue, over x and out viewed as
+// [M][hc][dim] bf16: boxes of 32 tokens x 1 stream x 64 channels (4 KB, one
+// 128-byte row per token) with the 128-byte swizzle.
+struct PairXMaps {
+  CUtensorMap x, out;
 };
 
 // Pair unit u -> (M pair p: M tiles 2p, 2p+1; N tile nt), rasterised in
@@ -996,12 +1018,220 @@ __device__ __forceinline__ int64_t pair_unit(const GemmArgs& a, int64_t u, int k
   return -1;
 }
 
-template <bool BULK>
+// Pair unit u of the fused mode: the fused order of fused_coords over M pairs,
+// whole K.
+template <bool FUSED>
+__device__ __forceinline__ int64_t pair_unit_of(const GemmArgs& a, int64_t u, int kbt, int& mp, int& nt, int& kb0,
+                                                int& kbn) {
+  if constexpr (FUSED) {
+    fused_coords(a, u, (a.m_tiles + 1) >> 1, mp, nt);
+    kb0 = 0;
+    kbn = kbt;
+    return -1;
+  }
+  return pair_unit(a, u, kbt, mp, nt, kb0, kbn);
+}
+
+// A fused-pair epilogue warp's x staging: kXBufs buffers filled in turn by
+// tensor copies that lane 0 issues; every lane waits for a chunk in the order
+// issued.  `issued` is lane 0's count, `used` every lane's.
+struct XStage {
+  uint8_t* base;
+  uint64_t* bars;
+  uint32_t issued;
+  uint32_t used;
+  __device__ __forceinline__ void issue(const CUtensorMap* map, uint32_t bytes, int32_t x, int32_t y, int32_t z) {
+    const uint32_t b = issued % kXBufs;
+    mbar_arrive_expect_tx(&bars[b], bytes);
+    tma_load_3d(base + b * kXBufBytes, map, &bars[b], x, y, z);
+    ++issued;
+  }
+  // the next chunk's shared address, once it has landed; false if the wait ran out
+  __device__ __forceinline__ bool wait(volatile int* abort_flag, uint32_t& addr) {
+    const uint32_t b = used % kXBufs;
+    const bool ok = mbar_wait(&bars[b], (used / kXBufs) & 1u, abort_flag);
+    addr = smem_u32(base + b * kXBufBytes);
+    ++used;
+    return __all_sync(0xFFFFFFFFu, ok);
+  }
+  // lane 0: let every copy still in flight land (leaving early)
+  __device__ __forceinline__ void drain() {
+    for (uint32_t k = used; k < issued; ++k)
+      mbar_wait(&bars[k % kXBufs], (k / kXBufs) & 1u, nullptr, kDrainLimitNs);
+    used = issued;
+  }
+};
+
+// Byte b of a staged box image sits at b with its 16-byte chunk index
+// (bits 4-6) xor-ed with bits 7-9: the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz128(uint32_t b) { return b ^ (((b >> 7) & 7u) << 4); }
+
+constexpr int kChunkCols = 64;                  // channels of one staged x chunk
+
+// Key tile of the fused pair epilogue: fused_key_epilogue's sums, in its order,
+// with row m's hidden state read from the staged chunks (the block's 4 chunks
+// of 64 channels; chunks 0 and 1 issued at the unit's start, chunk c + 2 once
+// chunk c is read).  Lane = row.
+__device__ __forceinline__ bool pair_key_epilogue(const GemmArgs& a, const CUtensorMap* tmx, uint32_t t_row,
+                                                  int64_t m0, int n0, int lane, float* wsm, XStage& xs,
+                                                  volatile int* abort_flag) {
+  const int s = n0 / a.dim;
+  const int d0 = n0 - s * a.dim;
+  const int64_t m = m0 + lane;
+  const bool active = m < a.M && (a.mask == nullptr || a.mask[m] != 0);
+  {
+    const float4* wg = reinterpret_cast<const float4*>(a.wprod + static_cast<int64_t>(s) * a.dim + d0) + 2 * lane;
+    reinterpret_cast<float4*>(wsm)[2 * lane] = __ldg(wg);
+    reinterpret_cast<float4*>(wsm)[2 * lane + 1] = __ldg(wg + 1);
+    __syncwarp();
+  }
+  float th[16], tk[16], td[16];   // the butterfly after its first step (registers: the loop is unrolled)
+#pragma unroll
+  for (int c = 0; c < kBN / kChunkCols; ++c) {
+    uint32_t xb;
+    if (!xs.wait(abort_flag, xb)) return false;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * kChunkCols + half * 32), r);
+      tmem_ld_wait();
+      if (active) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int j = 4 * half + g;                  // 16-byte chunk of the row's 128 bytes
+          const int l = 8 * c + j;                     // group index in the block
+          float h[8];
+          unpack8_bf16(ld_shared_v4(xb + swz128(static_cast<uint32_t>(lane * 128 + j * 16))), h);
+          const float4 w0 = reinterpret_cast<const float4*>(wsm)[2 * l];
+          const float4 w1 = reinterpret_cast<const float4*>(wsm)[2 * l + 1];
+          const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          float sh = 0.0f, sk = 0.0f, sd = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float k = round_bf16(__uint_as_float(r[8 * g + e]));
+            sh = fmaf(h[e], h[e], sh);
+            sk = fmaf(k, k, sk);
+            sd = fmaf(__fmul_rn(h[e], w[e]), k, sd);
+          }
+          if (l < 16) {
+            th[l] = sh; tk[l] = sk; td[l] = sd;
+          } else {                                     // butterfly step 16
+            th[l - 16] = th[l - 16] + sh; tk[l - 16] = tk[l - 16] + sk; td[l - 16] = td[l - 16] + sd;
+          }
+        }
+      }
+    }
+    __syncwarp();                                      // every lane has read the chunk
+    if (lane == 0 && c + 2 < kBN / kChunkCols)
+      xs.issue(tmx, kXBufBytes, d0 + (c + 2) * kChunkCols, s, static_cast<int32_t>(m0));
+  }
+  if (active) {
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+#pragma unroll
+      for (int l = 0; l < off; ++l) {
+        th[l] = th[l] + th[l + off]; tk[l] = tk[l] + tk[l + off]; td[l] = td[l] + td[l + off];
+      }
+    }
+    const int nblk = a.dim / kBN;
+    reinterpret_cast<float4*>(a.gsum)[(m * a.hc + s) * nblk + d0 / kBN] = make_float4(th[0], tk[0], td[0], 0.0f);
+  }
+  return true;
+}
+
+// Value tile of the fused pair epilogue: once the gates of the warp's 32 rows
+// are ready, out = h + gate * value, 64 channels of one stream per staged
+// chunk (chunk n: channels 64 (n / hc) .., stream n % hc), computed in place in
+// the chunk and written back by a tensor store (tokens past M are not
+// written; a masked token's row goes back as it came, x itself).  Lane = row.
+// Returns false if a wait ran out.
+__device__ __forceinline__ bool pair_value_epilogue(const GemmArgs& a, const CUtensorMap* tmx, const CUtensorMap* tmo,
+                                                    uint32_t t_row, int64_t m0, int mt, int q, int n0, int lane,
+                                                    XStage& xs, volatile int* abort_flag) {
+  const int d0 = n0 - a.hc * a.dim;
+  bool ok = true;
+  if (lane == 0) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (ld_acquire_u32(a.counters + mt * 8 + 4 + q) == 0u) {
+      if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  if (!ok) return false;
+  __threadfence();
+  const int64_t m = m0 + lane;
+  const bool mix = m < a.M && (a.mask == nullptr || a.mask[m] != 0);
+  float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mix) gv = __ldcg(reinterpret_cast<const float4*>(a.gates) + m);
+  const float gs[kMaxStreams] = {gv.x, gv.y, gv.z, gv.w};
+  const int nch = (kBN / kChunkCols) * a.hc;
+#pragma unroll 1
+  for (int c = 0; c < kBN / kChunkCols; ++c) {
+    float v[kChunkCols];                               // kv as the projection rounds it
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * kChunkCols + half * 32), r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[32 * half + e] = round_bf16(__uint_as_float(r[e]));
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxStreams; ++s) {
+      if (s >= a.hc) break;
+      const int n = c * a.hc + s;
+      uint32_t xb;
+      if (!xs.wait(abort_flag, xb)) return false;
+      if (mix) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t addr = xb + swz128(static_cast<uint32_t>(lane * 128 + j * 16));
+          float h[8];
+          unpack8_bf16(ld_shared_v4(addr), h);
+          const float* vv = v + 8 * j;
+          uint4 o;
+          o.x = pack_bf16x2(fmaf(gs[s], vv[0], h[0]), fmaf(gs[s], vv[1], h[1]));
+          o.y = pack_bf16x2(fmaf(gs[s], vv[2], h[2]), fmaf(gs[s], vv[3], h[3]));
+          o.z = pack_bf16x2(fmaf(gs[s], vv[4], h[4]), fmaf(gs[s], vv[5], h[5]));
+          o.w = pack_bf16x2(fmaf(gs[s], vv[6], h[6]), fmaf(gs[s], vv[7], h[7]));
+          st_shared_v4(addr, o);
+        }
+      }
+      fence_proxy_async_shared();                      // the chunk's new bytes, for the tensor store
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmo, xb, d0 + c * kChunkCols, s, static_cast<int32_t>(m0));
+        bulk_commit();
+        if (n + 2 < nch) {
+          const int n2 = n + 2;
+          bulk_wait_read_but_one();                    // chunk n - 1's store has read the buffer chunk n + 2 takes
+          xs.issue(tmx, kXBufBytes, d0 + (n2 / a.hc) * kChunkCols, n2 % a.hc, static_cast<int32_t>(m0));
+        }
+      }
+    }
+  }
+  return true;
+}
+
+// FUSED: the gate epilogue of wkv_gemm_kernel, on the pair's tiles.  Units
+// then come from the work-ticket counter: the even CTA's producer takes a
+// ticket and writes it into the unit queue of both CTAs (its own and, through
+// the cluster window, the odd CTA's); the even CTA's queue slot is free once
+// its MMA thread and epilogue warps and the odd CTA's producer and epilogue
+// warps have read it (10 arrivals on the even CTA's barrier).  Each CTA's
+// epilogue treats its 128 rows -- M tile 2p + rank -- as one M tile of the
+// one-CTA fused kernel, with x staged in shared memory by tensor copies (xm)
+// and the output written by tensor stores.
+template <bool BULK, bool FUSED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     wkv_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                         const GemmArgs a) {
-  using C = PairCfg;
-  constexpr int S = kPairStages;
+                         const __grid_constant__ PairXMaps xm, const GemmArgs a) {
+  using C = PairCfgT<FUSED>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;                             // stage s at s * kABytes
@@ -1013,8 +1243,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = bars + 2 * S;
   uint64_t* tempty = tfull + 2;                    // even CTA: 8 epilogue warps of the pair
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xbars = drain + 1;                     // fused: kXBufs per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbars + (FUSED ? 4 * kXBufs : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // fused mode: the unit queue (slot values, then the full and empty barriers)
+  volatile int64_t* ring = reinterpret_cast<volatile int64_t*>(smem + (FUSED ? C::kRingOffset : 0));
+  uint64_t* ufull = reinterpret_cast<uint64_t*>(smem + (FUSED ? C::kRingOffset : 0) + kRing * 8);
+  uint64_t* uempty = ufull + kRing;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1032,10 +1267,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[b], 8);
     }
     mbar_init(drain, 1);
+    if constexpr (FUSED) {
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(&ufull[i], 1);
+        mbar_init(&uempty[i], 10);
+      }
+      for (int i = 0; i < 4 * kXBufs; ++i) mbar_init(&xbars[i], 1);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
+    if constexpr (FUSED) {
+      tma_prefetch_desc(&xm.x);
+      tma_prefetch_desc(&xm.out);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -1048,6 +1294,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // fused mode: read the next unit from this CTA's queue and free the slot
+  // (on the even CTA's barrier); -2 if the wait ran out
+  uint32_t rslot = 0, rphase = 0;
+  auto next_queued = [&](bool one_lane) -> int64_t {
+    const bool got = rank == 0 ? mbar_wait(&ufull[rslot], rphase, abort_flag)
+                               : mbar_wait_cluster(&ufull[rslot], rphase, abort_flag);
+    const int64_t v = got ? ring[rslot] : -2;
+    if (one_lane) __syncwarp();
+    if (got && (!one_lane || lane == 0)) {
+      if (rank == 0) mbar_arrive(&uempty[rslot]);
+      else mbar_arrive_remote(mapa_shared(&uempty[rslot], 0));
+    }
+    if (++rslot == kRing) {
+      rslot = 0;
+      rphase ^= 1u;
+    }
+    return v;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
@@ -1059,10 +1324,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued[S] = {};
       bool ok = true;
+      // fused mode: the even CTA takes the pair's tickets and queues them in
+      // both CTAs (-1: no more units); the odd CTA reads its queue
+      auto take = [&]() -> int64_t {
+        if (rank != 0) return next_queued(false);
+        if (!mbar_wait_cluster(&uempty[rslot], rphase ^ 1u, abort_flag)) return -2;
+        const uint32_t t = atomicAdd(a.tickets, 1u);
+        const int64_t v = t < a.units ? static_cast<int64_t>(t) : -1;
+        ring[rslot] = v;
+        st_cluster_s64(mapa_shared(const_cast<int64_t*>(&ring[rslot]), 1), v);
+        mbar_arrive(&ufull[rslot]);
+        mbar_arrive_remote(mapa_shared(&ufull[rslot], 1));
+        if (++rslot == kRing) {
+          rslot = 0;
+          rphase ^= 1u;
+        }
+        return v;
+      };
+      int64_t u = pair;
+      if constexpr (FUSED) {
+        u = take();
+        if (u == -2) ok = false;
+      }
+      const int64_t first = u;
       int pre = 0;
-      if (pair < a.units) {                        // the weight halves of the first stages, before the wait
+      if (ok && u >= 0 && u < a.units) {           // the weight halves of the first stages, before the wait
         int mp, nt, kb0, kbn;
-        pair_unit(a, pair, kbt, mp, nt, kb0, kbn);
+        pair_unit_of<FUSED>(a, u, kbt, mp, nt, kb0, kbn);
         pre = min(S, kbn);
         for (int i = 0; i < pre; ++i) {
           if (rank == 0) mbar_arrive_expect_tx(&full[i], 2 * C::kStageBytes);
@@ -1071,13 +1359,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       grid_dependency_wait();                      // the gathered rows are written by the gather kernel
-      for (int64_t u = pair; u < a.units && ok; u += npairs) {
-        if (u + npairs >= a.units) grid_launch_dependents();
+      while (ok && u >= 0 && u < a.units) {
+        if (!FUSED && u + npairs >= a.units) grid_launch_dependents();
         int mp, nt, kb0, kbn;
-        pair_unit(a, u, kbt, mp, nt, kb0, kbn);
+        pair_unit_of<FUSED>(a, u, kbt, mp, nt, kb0, kbn);
         const int32_t row0 = mp * (2 * kBM) + static_cast<int32_t>(rank) * kBM;
         for (int kb = 0; kb < kbn; ++kb) {
-          if (!(u == pair && kb < pre)) {
+          if (!(u == first && kb < pre)) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
               ok = false;
               break;
@@ -1093,6 +1381,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             phase ^= 1u;
           }
         }
+        if (!ok) break;
+        if constexpr (FUSED) {
+          u = take();
+          if (u == -2) ok = false;
+        } else {
+          u += npairs;
+        }
       }
       if (!ok) {
         raise_abort(abort_flag, a.err);
@@ -1103,10 +1398,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     __syncwarp();
-  }
-  else if (warp == 1) {
+  } else if (warp == 1) {
     grid_dependency_wait();
-    if (lane == 0 && rank == 0) {
+    if (rank == 0 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer (even CTA)
       const uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN);
       int stage = 0;
@@ -1114,8 +1408,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t u = pair; u < a.units && ok; u += npairs) {
-        if (u + npairs >= a.units) grid_launch_dependents();
+      for (int64_t u = pair;; u += npairs) {
+        if constexpr (FUSED) {
+          u = next_queued(false);
+          if (u == -2) ok = false;
+          if (u < 0) break;
+        } else {
+          if (u >= a.units) break;
+          if (u + npairs >= a.units) grid_launch_dependents();
+        }
         if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -1123,7 +1424,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         int mp, nt, kb0, kbn;
-        pair_unit(a, u, kbt, mp, nt, kb0, kbn);
+        pair_unit_of<FUSED>(a, u, kbt, mp, nt, kb0, kbn);
         for (int kb = 0; kb < kbn; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
@@ -1158,23 +1459,73 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     grid_dependency_wait();
     const int q = warp & 3;
-    uint8_t* epi = smem + C::kEpiOffset + (warp - 2) * kPlainWarpBytes;
+    uint8_t* epi = smem + C::kEpiOffset + (warp - 2) * C::kEpiWarp;
     const uint32_t tempty_even[2] = {mapa_shared(&tempty[0], 0), mapa_shared(&tempty[1], 0)};
+    XStage xs{smem + C::kXOffset + (warp - 2) * kXBufs * kXBufBytes, xbars + (warp - 2) * kXBufs, 0u, 0u};
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int64_t u = pair; u < a.units; u += npairs) {
-      if (u + npairs >= a.units) grid_launch_dependents();
+    for (int64_t u = pair;; u += npairs) {
+      if constexpr (FUSED) {
+        u = next_queued(true);
+        if (u == -2) ok = false;
+        if (u < 0) break;
+      } else {
+        if (u >= a.units) break;
+        if (u + npairs >= a.units) grid_launch_dependents();
+      }
       int mp, nt, kb0, kbn;
-      const int64_t j = pair_unit(a, u, kbt, mp, nt, kb0, kbn);
+      const int64_t j = pair_unit_of<FUSED>(a, u, kbt, mp, nt, kb0, kbn);
+      const int mt = 2 * mp + static_cast<int>(rank);
+      const int64_t m0 = static_cast<int64_t>(mt) * kBM + q * 32;
+      // fused: whether this warp holds rows (the odd CTA of a last pair over an
+      // odd number of M tiles holds none, and the last M tile may end early)
+      const bool rows = mt < a.m_tiles && m0 < a.M;
+      if constexpr (FUSED) {
+        if (rows) {
+          // the unit's rows of x: asked of the L2 while the unit's MMAs run,
+          // and the first two chunks into the staging buffers
+          const int64_t mr = m0 + lane;
+          const bool key = nt < a.key_n_tiles;
+          const int s = key ? nt * kBN / a.dim : 0;
+          const int d0 = key ? nt * kBN - s * a.dim : (nt - a.key_n_tiles) * kBN;
+          if (mr < a.M) {
+            if (key) {
+              prefetch_l2(a.x + (mr * a.hc + s) * a.dim + d0, kBN * 2);
+            } else {
+              for (int t = 0; t < a.hc; ++t) prefetch_l2(a.x + (mr * a.hc + t) * a.dim + d0, kBN * 2);
+            }
+          }
+          if (lane == 0) {
+            bulk_wait_read_all();                  // the last unit's stores have read their buffers
+            for (int n = 0; n < 2; ++n) {          // key: chunk n of stream s; value: chunk n of the streams
+              if (key) xs.issue(&xm.x, kXBufBytes, d0 + n * kChunkCols, s, static_cast<int32_t>(m0));
+              else xs.issue(&xm.x, kXBufBytes, d0 + (n / a.hc) * kChunkCols, n % a.hc, static_cast<int32_t>(m0));
+            }
+          }
+        }
+      }
       if (!mbar_wait_cluster(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int64_t m0 = static_cast<int64_t>(mp) * (2 * kBM) + static_cast<int64_t>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      if (j >= 0) {
+      if constexpr (FUSED) {
+        if (rows) {
+          if (nt < a.key_n_tiles) {
+            if (!pair_key_epilogue(a, &xm.x, t_row, m0, nt * kBN, lane, reinterpret_cast<float*>(epi), xs,
+                                   abort_flag)) {
+              ok = false;
+              break;
+            }
+            fused_key_publish(a, m0 + lane, mt, q, lane);
+          } else if (!pair_value_epilogue(a, &xm.x, &xm.out, t_row, m0, mt, q, nt * kBN, lane, xs, abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
+      } else if (j >= 0) {
         // remainder range j % rem_splits of tile j / rem_splits: this CTA's
         // 128 rows of fp32 sums to the workspace, [tile][range][CTA][128][256]
         float* ws = a.rem_ws + ((j * 2 + rank) * kBM + q * 32) * kBN;
@@ -1194,6 +1545,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     if (!ok && lane == 0) raise_abort(abort_flag, a.err);
+    if constexpr (FUSED) {
+      if (lane == 0) {
+        xs.drain();                                // copies still in flight (leaving early)
+        bulk_wait_all();                           // the tensor stores are done
+      }
+    }
     __syncwarp();
   }
 
@@ -1205,6 +1562,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cluster_wait();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+  if constexpr (FUSED) {
+    // every even CTA has taken its last ticket; the last CTA here resets the
+    // counter for the next launch (no early launch of dependents, as in
+    // wkv_gemm_kernel's fused mode)
+    if (threadIdx.x == 0 && atom_acq_rel_add_u32(a.tickets + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.tickets, 0u);
+      atomicExch(a.tickets + 1, 0u);
+    }
+  }
 }
 
 template <int A_ROWS, int STAGES>
@@ -1378,11 +1744,14 @@ cudaError_t gemm_prepare() {
   if (e == cudaSuccess) e = set_smem_attr<64, 5>();
   if (e == cudaSuccess) e = set_smem_attr<32, 5>();
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(wkv_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(wkv_gemm_pair_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PairCfg::kSmemBytes));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(wkv_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(wkv_gemm_pair_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(PairCfg::kSmemBytes));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(wkv_gemm_pair_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(PairFusedCfg::kSmemBytes));
   return e;
 }
 
@@ -1399,7 +1768,7 @@ int gemm_pair_slots(int num_sms) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, wkv_gemm_pair_kernel<false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, wkv_gemm_pair_kernel<false, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1444,18 +1813,41 @@ cudaError_t launch_gemm(const void* rows, const CUtensorMap& tmB, const GemmArgs
     const cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(kBK * 2)};
     const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
     const cuuint32_t estr[2] = {1, 1};
-    if (a.fp8 || a.out_mode != kOutBf16 || a.wpack == nullptr || (ctas & 1) != 0 || enc == nullptr ||
+    const bool fused = a.out_mode == kOutFused;
+    if (a.fp8 || (a.out_mode != kOutBf16 && !fused) || a.wpack == nullptr || (ctas & 1) != 0 || enc == nullptr ||
+        (fused && a.rem_splits != 0) ||
         !make_tmap_bf16(&tmA, rows, static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.K), kBM) ||
         enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(a.wpack), wdims, wstrides, wbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(ctas));
+    PairXMaps xm;
+    std::memset(&xm, 0, sizeof(xm));
+    if (fused) {
+      // x and out as [M][hc][dim] bf16, boxes of 64 channels x 1 stream x 32
+      // tokens: 128 bytes per token, the 128-byte swizzle's row (the box's
+      // inner extent is exactly the swizzle span)
+      const cuuint64_t xdims[3] = {static_cast<cuuint64_t>(a.dim), static_cast<cuuint64_t>(a.hc),
+                                   static_cast<cuuint64_t>(a.M)};
+      const cuuint64_t xstrides[2] = {static_cast<cuuint64_t>(a.dim) * 2, static_cast<cuuint64_t>(a.hc) * a.dim * 2};
+      const cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunkCols), 1, 32};
+      const cuuint32_t estr3[3] = {1, 1, 1};
+      auto enc3 = [&](CUtensorMap* m, const void* base) {
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), xdims, xstrides, box, estr3,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      };
+      if (a.hc < 1 || a.hc > kMaxStreams || a.dim % kBN != 0 || !enc3(&xm.x, a.x) || !enc3(&xm.out, a.out))
+        return cudaErrorInvalidValue;
+      return launch_pdl(wkv_gemm_pair_kernel<false, true>, grid, dim3(kGemmThreads), PairFusedCfg::kSmemBytes, stream,
+                        2, tmA, tmW, xm, a);
+    }
     if (a.bulk_epilogue)
-      return launch_pdl(wkv_gemm_pair_kernel<true>, grid, dim3(kGemmThreads), PairCfg::kSmemBytes, stream, 2, tmA,
-                        tmW, a);
-    return launch_pdl(wkv_gemm_pair_kernel<false>, grid, dim3(kGemmThreads), PairCfg::kSmemBytes, stream, 2, tmA,
-                      tmW, a);
+      return launch_pdl(wkv_gemm_pair_kernel<true, false>, grid, dim3(kGemmThreads), PairCfg::kSmemBytes, stream, 2,
+                        tmA, tmW, xm, a);
+    return launch_pdl(wkv_gemm_pair_kernel<false, false>, grid, dim3(kGemmThreads), PairCfg::kSmemBytes, stream, 2,
+                      tmA, tmW, xm, a);
   }
   const int ar = gemm_a_rows(a.M);
   CUtensorMap tmA;

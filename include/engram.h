@@ -108,7 +108,9 @@ typedef struct {
                            projection runs without split-K: 1 = in the projection's epilogue
                            (kv never reaches HBM), -1 = in a separate kernel that reads kv,
                            0 = the library chooses by batch size (the way that measured
-                           faster on GB300).  Same bits either way, and the same as
+                           faster on GB300: the epilogue of the CTA-pair projection from
+                           1,024 tokens on, when all SMs are the projection's; the separate
+                           kernel otherwise).  Same bits either way, and the same as
                            engram_lookup_project + engram_gate_apply: a batch that takes the
                            fused epilogue keeps whole tiles in its plan (no remainder split,
                            see engram_plan), so that both ways sum kv alike.  The fused
@@ -116,7 +118,9 @@ typedef struct {
                            an M tile's key tiles come well before its value tiles, whose
                            epilogues wait (bounded) for the gates the key tiles form: only
                            running CTAs take tiles, so the wait never depends on a CTA that
-                           has not started, whatever else shares the GPU. */
+                           has not started, whatever else shares the GPU.  On CTA pairs the
+                           epilogue warps stage x in shared memory by tensor copies and write
+                           the output by tensor stores. */
   int32_t wkv_fmt;      /* engram_wkv_fmt; ENGRAM_WKV_MXFP8 needs K a multiple of 128 and
                            takes no fused epilogue (fuse_gate is ignored) */
   int64_t row_offset;   /* global id of the table's first row, >= 0: the table holds rows
@@ -230,7 +234,8 @@ ENGRAM_API engram_status engram_plan(const engram_ctx* ctx, int64_t m_tokens, in
  * last wave of the grid, the plan also cuts those last tiles into 2-4 K ranges
  * whose fp32 sums a small kernel after the projection adds up in range order;
  * this changes kv's summation order for those tiles, not its tolerance.
- * Contexts with max_tokens <= 128 or fuse_gate set keep whole tiles.) */
+ * Contexts with max_tokens <= 128, and batches that take the fused gate
+ * epilogue, keep whole tiles.) */
 
 /* The projection's whole plan for B*T = m_tokens on this context (queues
  * nothing).  ENGRAM_EINVAL for a NULL context or pointer or a negative count. */

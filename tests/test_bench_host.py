@@ -56,6 +56,8 @@ def test_recorded_traffic_matches_workload_digest_and_plan(tmp_path, monkeypatch
     pairs = bench.plan_key(dict(splits=1, ctas=152, cta_pairs=1, rem_tiles=16, rem_splits=4))
     assert pairs == "1x152pr16x4" and bench.recorded_traffic("w4", pairs) == 7.0
     assert bench.recorded_traffic("w4", "1x152p") is None         # pairs without the remainder split
+    fused = bench.plan_key(dict(splits=1, ctas=152, cta_pairs=1, rem_tiles=0, rem_splits=0, fused_gate=1))
+    assert fused == "1x152pf" and bench.recorded_traffic("w4", fused) is None
 
 
 def test_committed_traffic_records_add_up():

@@ -195,9 +195,12 @@ def test_empty_batch_is_a_no_op(tiny):
 def test_fused_epilogue_matches_split_path(tiny, B, T, mask_frac):
     """fuse_gate: the gate and residual add run in the projection's epilogue
     (plans without split-K); the result must equal lookup_project + gate_apply
-    bit for bit, and match the oracle.  2,300 and 4,200 tokens span 18 and 33
-    M tiles: several groups of 16 in the fused unit order (key tiles of a
-    group, then the value tiles of the group before), the last one partial."""
+    bit for bit, and match the oracle.  Below 256 tokens the one-CTA kernel
+    runs it, from 256 on the CTA-pair kernel (300 and 4,200 tokens: an odd
+    number of M tiles, so the last pair's second CTA holds no rows).  2,300
+    and 4,200 tokens span 18 and 33 M tiles: several groups of 16 M tiles (8
+    pairs) in the fused unit order (key tiles of a group, then the value
+    tiles of the group before), the last one partial."""
     from engram_hashed_gram_gb300.layer import EngramLayer
     dev = tiny["dev"]
     fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=4200,
@@ -213,6 +216,9 @@ def test_fused_epilogue_matches_split_path(tiny, B, T, mask_frac):
     fused.forward(ids, inplace, mask, out=inplace)
     assert fused.sync_status()[0] == 0
     assert fused.plan(B * T)[0] == 1                      # the fused epilogue needs a plan without split-K
+    info = fused.describe_plan(B * T)
+    assert info["fused_gate"] == 1 and info["rem_splits"] == 0
+    assert info["cta_pairs"] == (1 if B * T >= 256 else 0)
     assert torch.equal(out.view(torch.int16), split.view(torch.int16))
     assert torch.equal(out.view(torch.int16), again.view(torch.int16))
     assert torch.equal(out.view(torch.int16), inplace.view(torch.int16))
@@ -255,21 +261,24 @@ def test_stream_gate_kernel_matches_cluster_kernel(tiny):
     print(summary)
 
 
-def test_bounded_wait_runs_out_and_the_context_recovers(tiny):
+@pytest.mark.parametrize("T", [200, 600])
+def test_bounded_wait_runs_out_and_the_context_recovers(tiny, T):
     """Failure detection without a fault: with the test hook, the fused
     epilogue never raises its gates-ready flags, the value tiles' bounded wait
     (two seconds) runs out, every role of the projection leaves its loop, and
     engram_sync_status() reports ENGRAM_ETIMEOUT.  The next call on the same
-    context is correct again (equal to its lookup_project + gate_apply)."""
+    context is correct again (equal to its lookup_project + gate_apply).
+    200 tokens run the one-CTA kernel, 600 the CTA-pair kernel."""
     import time
     from engram_hashed_gram_gb300 import _lib
     from engram_hashed_gram_gb300.layer import EngramLayer
-    w, inp = _inputs(tiny, 1, 200, seed=6)
+    w, inp = _inputs(tiny, 1, T, seed=6)
     ids, x, _ = _dev(inp)
     dev = tiny["dev"]
-    fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=256, fuse_gate=True)
+    fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=T, fuse_gate=True)
     try:
-        assert fused.plan(200)[0] == 1                       # single pass: the fused epilogue runs
+        assert fused.plan(T)[0] == 1                         # single pass: the fused epilogue runs
+        assert fused.describe_plan(T)["cta_pairs"] == (1 if T >= 256 else 0)
         assert _lib.engram().engram_test_hook(fused._ctx, _lib.TEST_HOLD_GATE_FLAGS) == 0
         t0 = time.perf_counter()
         fused.forward(ids, x)
@@ -335,10 +344,12 @@ def test_remainder_split_tiles(tiny):
         gates = torch.empty((2, 650, 4), dtype=torch.float32, device="cuda")
         split = layer.gate_apply(kv, x, mask, gates=gates)
         assert layer.sync_status()[0] == 0
-        # on all SMs this batch takes CTA pairs (whole 256 x 256 tiles); on 137
-        # SMs the one-CTA plan cuts the 4 tiles of its last wave into K ranges
+        # on all SMs this batch takes CTA pairs (whole 256 x 256 tiles) with the
+        # gate in their epilogue; on 137 SMs the one-CTA plan with the separate
+        # gate kernel cuts the 4 tiles of its last wave into K ranges
         assert layer.plan(1300) == (1, 152)
-        assert layer.forward_kernels(1300) == 3
+        assert layer.forward_kernels(1300) == 2
+        assert torch.equal(out.view(torch.int16), split.view(torch.int16))
         layer.set_sm_budget(137)
         assert layer.plan(1300) == (1, 137)
         # gather, projection, the remainder's sums, gate; no remainder at 1,233 tokens (9 full waves)
@@ -366,12 +377,14 @@ def test_cta_pair_projection(tiny, B, T):
     pair without a row of the batch; 1,750 tokens make 700 pair tiles, 16 more
     than 9 waves of 76 pairs, which the plan cuts into K ranges).  Held to 150
     SMs the same batch takes the one-CTA kernel: both are checked against the
-    oracle on every token, and their kv agree within the dot-product bound."""
+    oracle on every token, and their kv agree within the dot-product bound.
+    (The separate gate kernel throughout: the fused epilogue has its own tests.)"""
     from engram_hashed_gram_gb300.layer import EngramLayer
     w, inp = _inputs(tiny, B, T, mask_frac=0.1, seed=12)
     ids, x, mask = _dev(inp)
     dev = tiny["dev"]
-    layer = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=2048)
+    layer = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=2048,
+                        fuse_gate=False)
     M = B * T
     if M == 1750:
         assert layer.forward_kernels(M) == 4           # gather, pairs, the remainder's sums, gate
@@ -397,3 +410,35 @@ def test_cta_pair_projection(tiny, B, T):
     diff = np.abs(O.bf16_value(res[0]) - O.bf16_value(res[150]))
     assert np.all(diff <= 2 * bound)
     print(f"{M} tokens: pair vs one-CTA kv identical in {float((diff == 0).mean()):.6f} of the elements")
+
+
+def test_library_choice_fuses_large_batches_on_pairs(tiny):
+    """fuse_gate left to the library: from 1,024 tokens on, with all SMs, the
+    gate and the residual add run in the CTA-pair projection's epilogue (two
+    kernels per forward); below that, or held to fewer SMs, the separate gate
+    kernel.  The fused forward equals lookup_project + gate_apply bit for bit
+    and matches the oracle on every token."""
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    dev = tiny["dev"]
+    layer = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=2048)
+    try:
+        assert layer.describe_plan(512)["fused_gate"] == 0 and layer.describe_plan(512)["cta_pairs"] == 1
+        info = layer.describe_plan(1200)
+        assert info["fused_gate"] == 1 and info["cta_pairs"] == 1 and info["rem_splits"] == 0
+        assert layer.forward_kernels(1200) == 2
+        layer.set_sm_budget(150)
+        assert layer.describe_plan(1200)["fused_gate"] == 0 and layer.describe_plan(1200)["cta_pairs"] == 0
+        layer.set_sm_budget(0)
+        B, T = 2, 600
+        w, inp = _inputs(tiny, B, T, mask_frac=0.1, seed=31)
+        ids, x, mask = _dev(inp)
+        out = layer.forward(ids, x, mask)
+        kv = layer.lookup_project(ids)
+        gates = torch.empty((B, T, 4), dtype=torch.float32, device="cuda")
+        split = layer.gate_apply(kv, x, mask, gates=gates)
+        assert layer.sync_status()[0] == 0
+        assert torch.equal(out.view(torch.int16), split.view(torch.int16))
+        P.check_layer(w, inp, np.arange(B * T), SD.device_bits(out), gates.cpu().numpy(), SD.device_bits(kv),
+                      "library choice, 1200 tokens")
+    finally:
+        layer.close()
