@@ -373,20 +373,19 @@ def run_ours(args, w, rank, world, local_rank):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
 
-    # ---- per-kernel durations: the same steps again with an event between the
-    # kernels (events between kernels also stop them from overlapping, so these
-    # are each kernel's own duration, and they are not used for `value`).  Each
-    # timed step directly follows an untimed one, as in the timed region, so
-    # that the GPU does not idle (and change its clocks) just before it.
-    stages = []
+    # ---- per-kernel durations: the timed region's steps again, queued the same
+    # way (flush + forward, the host ahead of the device), with an event
+    # between the kernels.  Events between kernels also stop them from
+    # overlapping, so these are each kernel's own duration; they are not used
+    # for `value`.
+    layer.enable_stage_timing(True, calls=args.steps)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e7 + 2e5 * args.steps))
     for i in range(args.steps):
         flush()
         layer.forward(ids, x, mask, out=out)
-        flush()
-        layer.enable_stage_timing(True)
-        layer.forward(ids, x, mask, out=out)
-        stages.append(layer.stage_times())       # waits for this step's last event
-        layer.enable_stage_timing(False)
+    stages = layer.stage_times_n(args.steps)      # waits for the last step's last event
+    layer.enable_stage_timing(False)
 
     # keep the GPU busy a little longer so the clock sampler sees the load
     t_end = time.perf_counter() + 1.0

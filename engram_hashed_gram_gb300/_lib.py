@@ -107,6 +107,7 @@ ENGRAM_FUNCS = {
                               c_void_p, c_int64, c_void_p, c_int64, c_int64, c_void_p]),
     "engram_enable_stage_timing": (c_int32, [c_void_p, c_int32]),
     "engram_stage_times": (c_int32, [c_void_p, POINTER(c_float)]),
+    "engram_stage_times_n": (c_int32, [c_void_p, c_int32, POINTER(c_float)]),
     "engram_status_string": (c_char_p, [c_int32]),
     "engram_abi_version": (c_int32, []),
 }

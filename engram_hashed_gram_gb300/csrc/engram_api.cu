@@ -45,7 +45,9 @@ struct engram_ctx {
   uint8_t* codes;             // fp8: [max_tokens, K] gathered e4m3 codes
   uint8_t* sfa;               // fp8: [ceil(max_tokens/128), K/128, 512] gathered scales
   CUtensorMap tmW;
-  cudaEvent_t ev[4];          // stage timing (null unless enabled)
+  cudaEvent_t* ev;            // stage timing: 4 events per remembered call (null unless enabled)
+  int32_t timing_sets;        // calls remembered
+  int64_t timing_calls;       // calls timed since enabled
   bool timing;
 };
 
@@ -71,6 +73,7 @@ constexpr int kMaxRemSplits = 4;
 
 // engram_config.fuse_gate: 0 = the library decides by batch size, 1 = the
 // fused gate epilogue whenever the plan allows it, -1 = never.
+constexpr int32_t kMaxTimedCalls = 4096;     // calls engram_enable_stage_timing can remember
 constexpr int32_t kFuseAuto = 0;
 constexpr int32_t kFuseAlways = 1;
 
@@ -228,15 +231,23 @@ engram_status check_tokens(const engram_ctx* c, int64_t B, int64_t T, int64_t* M
 
 engram_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ECUDA; }
 
+// Stage event i (0: before the gather, 1-3: after each stage) of the current
+// call; event 3 ends the call.
 void mark(engram_ctx* c, int i, cudaStream_t s) {
-  if (c->timing) cudaEventRecord(c->ev[i], s);
+  if (!c->timing) return;
+  cudaEventRecord(c->ev[(c->timing_calls % c->timing_sets) * 4 + i], s);
+  if (i == 3) ++c->timing_calls;
 }
 
 void destroy_events(engram_ctx* c) {
-  for (auto& e : c->ev) {
-    if (e != nullptr) cudaEventDestroy(e);
-    e = nullptr;
+  if (c->ev != nullptr) {
+    for (int64_t i = 0; i < 4 * static_cast<int64_t>(c->timing_sets); ++i)
+      if (c->ev[i] != nullptr) cudaEventDestroy(c->ev[i]);
+    delete[] c->ev;
   }
+  c->ev = nullptr;
+  c->timing_sets = 0;
+  c->timing_calls = 0;
   c->timing = false;
 }
 
@@ -446,7 +457,7 @@ const char* engram_status_string(engram_status s) {
   return "unknown status";
 }
 
-int32_t engram_abi_version(void) { return 104; }
+int32_t engram_abi_version(void) { return 105; }
 
 engram_status engram_create(engram_ctx** out, const engram_config* cfg, const engram_weights* w) {
   if (out == nullptr || cfg == nullptr || w == nullptr) return ENGRAM_EINVAL;
@@ -647,12 +658,15 @@ engram_status engram_sync_status(engram_ctx* ctx, engram_stream_t stream, int64_
 }
 
 engram_status engram_enable_stage_timing(engram_ctx* ctx, int32_t enable) {
-  if (ctx == nullptr) return ENGRAM_EINVAL;
+  if (ctx == nullptr || enable < 0 || enable > kMaxTimedCalls) return ENGRAM_EINVAL;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return ENGRAM_ECUDA;
   destroy_events(ctx);
-  if (!enable) return ENGRAM_OK;
-  for (auto& e : ctx->ev) {
-    if (cudaEventCreate(&e) != cudaSuccess) {
+  if (enable == 0) return ENGRAM_OK;
+  ctx->ev = new (std::nothrow) cudaEvent_t[4 * static_cast<size_t>(enable)]();
+  if (ctx->ev == nullptr) return ENGRAM_ENOMEM;
+  ctx->timing_sets = enable;
+  for (int64_t i = 0; i < 4 * static_cast<int64_t>(enable); ++i) {
+    if (cudaEventCreate(&ctx->ev[i]) != cudaSuccess) {
       destroy_events(ctx);
       return ENGRAM_ECUDA;
     }
@@ -661,13 +675,21 @@ engram_status engram_enable_stage_timing(engram_ctx* ctx, int32_t enable) {
   return ENGRAM_OK;
 }
 
-engram_status engram_stage_times(engram_ctx* ctx, float* ms) {
-  if (ctx == nullptr || ms == nullptr || !ctx->timing) return ENGRAM_EINVAL;
-  if (cudaEventSynchronize(ctx->ev[3]) != cudaSuccess) return ENGRAM_ECUDA;
-  for (int i = 0; i < 3; ++i)
-    if (cudaEventElapsedTime(&ms[i], ctx->ev[i], ctx->ev[i + 1]) != cudaSuccess) return ENGRAM_ECUDA;
+engram_status engram_stage_times_n(engram_ctx* ctx, int32_t n, float* ms) {
+  if (ctx == nullptr || ms == nullptr || !ctx->timing || n < 1 || n > ctx->timing_sets ||
+      n > ctx->timing_calls)
+    return ENGRAM_EINVAL;
+  const int64_t last = ctx->timing_calls - 1;
+  if (cudaEventSynchronize(ctx->ev[(last % ctx->timing_sets) * 4 + 3]) != cudaSuccess) return ENGRAM_ECUDA;
+  for (int32_t k = 0; k < n; ++k) {
+    const cudaEvent_t* e = ctx->ev + ((last - (n - 1) + k) % ctx->timing_sets) * 4;
+    for (int i = 0; i < 3; ++i)
+      if (cudaEventElapsedTime(&ms[3 * k + i], e[i], e[i + 1]) != cudaSuccess) return ENGRAM_ECUDA;
+  }
   return ENGRAM_OK;
 }
+
+engram_status engram_stage_times(engram_ctx* ctx, float* ms) { return engram_stage_times_n(ctx, 1, ms); }
 
 engram_status engram_test_hook(engram_ctx* ctx, int32_t hooks) {
   if (ctx == nullptr || (hooks & ~ENGRAM_TEST_HOLD_GATE_FLAGS) != 0) return ENGRAM_EINVAL;

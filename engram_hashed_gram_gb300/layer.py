@@ -209,8 +209,11 @@ class EngramLayer:
         """At most `sms` SMs for the projection's grid (0 = all of them)."""
         check(self._lib.engram_set_sm_budget(self._ctx, sms), "engram_set_sm_budget")
 
-    def enable_stage_timing(self, enable=True):
-        check(self._lib.engram_enable_stage_timing(self._ctx, 1 if enable else 0), "engram_enable_stage_timing")
+    def enable_stage_timing(self, enable=True, calls=1):
+        """Records stage events for the last `calls` forward / lookup_project
+        calls (engram_enable_stage_timing); enable=False drops them."""
+        n = int(calls) if enable else 0
+        check(self._lib.engram_enable_stage_timing(self._ctx, n), "engram_enable_stage_timing")
 
     def stage_times(self):
         """(gather, projection, gate) milliseconds of the last forward /
@@ -218,6 +221,12 @@ class EngramLayer:
         ms = (ctypes.c_float * 3)()
         check(self._lib.engram_stage_times(self._ctx, ms), "engram_stage_times")
         return tuple(ms)
+
+    def stage_times_n(self, n):
+        """[(gather, projection, gate)] milliseconds of the last n calls, oldest first."""
+        ms = (ctypes.c_float * (3 * n))()
+        check(self._lib.engram_stage_times_n(self._ctx, n, ms), "engram_stage_times_n")
+        return [tuple(ms[3 * i:3 * i + 3]) for i in range(n)]
 
     def close(self):
         if getattr(self, "_ctx", None) is not None and self._ctx.value:

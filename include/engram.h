@@ -274,15 +274,24 @@ ENGRAM_API engram_status engram_set_sm_budget(engram_ctx* ctx, int32_t sms);
 #define ENGRAM_TEST_HOLD_GATE_FLAGS 1
 ENGRAM_API engram_status engram_test_hook(engram_ctx* ctx, int32_t hooks);
 
-/* Stage timing, for benchmarks.  With enable != 0 the context creates CUDA
- * events and every later engram_forward / engram_lookup_project records one
- * before the gather and one after each of its kernels on the call's stream;
- * enable == 0 destroys them.  engram_stage_times() waits for the last
- * recorded event and writes the durations of the last call's stages in
- * milliseconds: ms[0] gather + dequantise, ms[1] projection, ms[2] gate and
- * residual add (or the split-K reduction, for lookup_project). */
+/* Stage timing, for benchmarks.  With enable = n > 0 the context creates CUDA
+ * events for its last n calls (n <= 4096) and every later engram_forward /
+ * engram_lookup_project records one before the gather and one after each of
+ * its kernels on the call's stream, cycling through the n sets; enable == 0
+ * destroys them (and a new enable starts the count afresh).  Events between
+ * the kernels keep them from overlapping, so these are each kernel's own
+ * durations.  engram_stage_times() waits for the last recorded event and
+ * writes the durations of the last call's stages in milliseconds: ms[0]
+ * gather + dequantise, ms[1] projection, ms[2] gate and residual add (the
+ * split-K reduction, for lookup_project; ~0 when the gate ran in the
+ * projection's epilogue).  engram_stage_times_n() does the same for the last
+ * n calls, oldest first, into ms[3 * n]: queued back to back, they time the
+ * kernels in the steady state of a run of calls.  ENGRAM_EINVAL for a NULL
+ * context or pointer, timing not enabled, or n outside [1, calls timed]
+ * (at most the n given to enable). */
 ENGRAM_API engram_status engram_enable_stage_timing(engram_ctx* ctx, int32_t enable);
 ENGRAM_API engram_status engram_stage_times(engram_ctx* ctx, float* ms);
+ENGRAM_API engram_status engram_stage_times_n(engram_ctx* ctx, int32_t n, float* ms);
 
 /* ---- n-gram hash: the step before the layer ----------------------------------
  * The hash `forward` excerpt of atlas.klimoza.dev "deepseek-v4.1 / engram-second"

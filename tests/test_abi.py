@@ -97,7 +97,7 @@ int main(void) {
 
 def test_host_only_entry_points(libs):
     lib = libs.engram()
-    assert lib.engram_abi_version() == 104
+    assert lib.engram_abi_version() == 105
     for code, text in ((0, b"ok"), (-1, b"invalid argument"), (-4, b"hash id outside the table"),
                        (-5, b"kernel wait timed out"), (-6, b"unsupported shape or format"), (7, b"unknown status")):
         assert lib.engram_status_string(code) == text
@@ -120,6 +120,7 @@ def test_host_only_entry_points(libs):
     assert lib.engram_test_hook(None, 1) == -1
     assert lib.engram_enable_stage_timing(None, 1) == -1
     assert lib.engram_stage_times(None, None) == -1
+    assert lib.engram_stage_times_n(None, 1, None) == -1
     assert lib.engram_hash(None, None, None, None, None, None, None, None, 0, None, 1, 1, None) == -1
     # more primes than the kernel's shared-memory table holds, refused before any CUDA call
     hc = libs.EngramHashConfig(n_layers=97, max_ngram_size=3, n_heads=32, max_batch=1, max_len=1, vocab_size=1,
