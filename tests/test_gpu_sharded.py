@@ -28,7 +28,7 @@ def env():
     B.build()
     from engram_hashed_gram_gb300 import synth_device as SD
     from engram_hashed_gram_gb300.layer import EngramLayer, shard_rows
-    w = dataclasses.replace(synth.workload("tiny_1x16"), B=1, T=300, mask="span10")
+    w = dataclasses.replace(synth.workload("tiny_1x16"), B=1, T=1200, mask="span10")
     table, scale = SD.make_table(w)
     inp = synth.make_inputs(w)
     d = SD.upload_inputs(inp)
@@ -63,9 +63,13 @@ def test_shard_rows_sum_to_the_whole_lookup(env):
         assert np.array_equal(SD.device_bits(p).reshape(ref.shape), ref)
 
 
-def test_forward_rows_on_the_exchanged_rows_equals_forward(env):
-    ids, d = env["ids"], env["d"]
-    x, mask = d["x"], d["mask"]
+@pytest.mark.parametrize("T", [1200, 300])
+def test_forward_rows_on_the_exchanged_rows_equals_forward(env, T):
+    """1,200 tokens run the CTA-pair projection with the gate in its epilogue,
+    300 tokens the CTA-pair projection and the separate gate kernel."""
+    ids, d = env["ids"][:, :T].contiguous(), env["d"]
+    x, mask = d["x"][:, :T].contiguous(), d["mask"][:, :T].contiguous()
+    assert env["whole"].describe_plan(T)["fused_gate"] == (1 if T >= 1024 else 0)
     parts = [lay.lookup(ids) for _, _, lay in env["shards"]]
     rows = (parts[0].view(torch.int32) + parts[1].view(torch.int32)).view(torch.bfloat16)
     for s, e, lay in env["shards"]:           # every rank gets the whole output from the exchanged rows
