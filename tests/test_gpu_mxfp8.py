@@ -106,7 +106,7 @@ def _kv_report(err, bound):
 
 
 @pytest.mark.parametrize("budget", [0, 64])
-@pytest.mark.parametrize("B,T", [(1, 16), (64, 1), (2, 100), (1, 300)])
+@pytest.mark.parametrize("B,T", [(1, 16), (64, 1), (2, 100), (1, 300), (1, 512)])
 def test_fp8_projection_kv(mx, B, T, budget):
     """lookup_project with the MXFP8 weight against the oracle's
     project_mxfp8, element by element (whole-K plans; split-K plans with the
@@ -134,7 +134,8 @@ def test_fp8_projection_kv(mx, B, T, budget):
     print(f"B={B} T={T} plan={plan} kv differing from the oracle: {float((err > 0).mean()):.4f}")
 
 
-@pytest.mark.parametrize("B,T,mask_frac", [(1, 16, 0.0), (64, 1, 0.2), (3, 70, 0.1), (200, 1, 0.0)])
+@pytest.mark.parametrize("B,T,mask_frac", [(1, 16, 0.0), (64, 1, 0.2), (3, 70, 0.1), (200, 1, 0.0), (1, 300, 0.1),
+                                           (2, 256, 0.05)])
 def test_fp8_forward_matches_oracle(mx, B, T, mask_frac):
     w, inp = _inputs(mx, B, T, mask_frac, seed=1)
     ids, x, mask = _dev(inp)
@@ -209,3 +210,40 @@ def test_fp8_configuration_errors(mx):
     rc = eng.engram_forward_noalloc(ctypes.byref(cfg), ctypes.byref(ws), ids.data_ptr(), x.data_ptr(), None,
                                     out.data_ptr(), 1, 1, torch.cuda.current_stream().cuda_stream)
     assert rc == lib.ENGRAM_EUNSUPPORTED
+
+
+def test_fp8_remainder_split(mx):
+    """2,500 tokens with the MXFP8 weight: 20 M tiles x 100 N tiles = 2,000
+    tiles on 152 SMs, 24 more than 13 waves, which the plan cuts into K
+    ranges (fp32 sums to the workspace, reduced in range order).  Every token
+    against the oracle (kv within the dot-product bound, gates and outputs by
+    the stage-wise check), and forward equal to lookup_project + gate_apply
+    bit for bit."""
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    dev = mx["dev"]
+    B, T = 1, 2500
+    layer = EngramLayer(mx["table"], mx["scale"], dev["wkv"], dev["q"], dev["k"], wkv_scale=dev["wkv_scale"],
+                        **dict(mx["kw"], max_tokens=2560))
+    try:
+        info = layer.describe_plan(B * T)
+        assert info["cta_pairs"] == 0 and info["rem_tiles"] == 24 and info["rem_splits"] >= 2 and info["fused_gate"] == 0
+        w, inp = _inputs(mx, B, T, mask_frac=0.05, seed=3, bad_ids=4)
+        ids, x, mask = _dev(inp)
+        out = layer.forward(ids, x, mask)
+        kv = layer.lookup_project(ids)
+        gates = torch.empty((B, T, 4), dtype=torch.float32, device="cuda")
+        split = layer.gate_apply(kv, x, mask, gates=gates)
+        st, _ = layer.sync_status()
+        assert st == 0
+        assert torch.equal(out.view(torch.int16), split.view(torch.int16))
+        M = B * T
+        summary = P.check_layer(w, inp, np.arange(M), SD.device_bits(out), gates.cpu().numpy(), SD.device_bits(kv),
+                                "fp8 2500 tokens")
+        e = P.oracle_rows(w, inp, np.arange(M))
+        ref = O.project_mxfp8(e, inp.wkv, inp.wkv_scale)
+        bound = P.kv_bound(e, P.weight_values(inp), ref, w.K, splits=8)
+        err = np.abs(O.bf16_value(SD.device_bits(kv).reshape(M, -1)) - O.bf16_value(ref))
+        assert np.all(err <= bound), _kv_report(err, bound)
+        print(summary)
+    finally:
+        layer.close()
