@@ -1396,7 +1396,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {
         raise_abort(abort_flag, a.err);
-        // the even CTA waits for the copies in flight (they count on its barriers)
+        // the even CTA waits for the copies in flight (they count on its
+        // barriers).  The odd CTA's are among them: both producers refill a
+        // stage only once its free barrier completes, and one multicast commit
+        // completes it in both CTAs at once; a wait runs out only after the
+        // MMA thread has stopped committing, so both have refilled the same
+        // stages.
         if (rank == 0)
           for (int i = 0; i < S; ++i)
             if (issued[i] > 0) mbar_wait(&full[i], (issued[i] - 1u) & 1u, nullptr, kDrainLimitNs);
