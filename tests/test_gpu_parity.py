@@ -442,3 +442,29 @@ def test_library_choice_fuses_large_batches_on_pairs(tiny):
                       "library choice, 1200 tokens")
     finally:
         layer.close()
+
+
+def test_stage_timing_over_a_run_of_calls(tiny):
+    """engram_enable_stage_timing(ctx, n) keeps the stage events of the last n
+    calls: after five forwards with n = 3, stage_times_n(3) gives three
+    (gather, projection, gate) triples of positive durations, the last equal
+    to stage_times(); asking for more calls than remembered is refused."""
+    from engram_hashed_gram_gb300._lib import EngramError
+    layer = tiny["layer"]
+    w, inp = _inputs(tiny, 1, 300, seed=14)
+    ids, x, mask = _dev(inp)
+    layer.enable_stage_timing(True, calls=3)
+    try:
+        with pytest.raises(EngramError):
+            layer.stage_times_n(1)                       # nothing timed yet
+        for _ in range(5):
+            layer.forward(ids, x, mask)
+        runs = layer.stage_times_n(3)
+        last = layer.stage_times()
+        assert len(runs) == 3 and runs[-1] == last
+        assert all(g > 0 and p > 0 and t > 0 for g, p, t in runs)
+        with pytest.raises(EngramError):
+            layer.stage_times_n(4)
+    finally:
+        layer.enable_stage_timing(False)
+    assert layer.sync_status()[0] == 0
