@@ -468,3 +468,34 @@ def test_stage_timing_over_a_run_of_calls(tiny):
     finally:
         layer.enable_stage_timing(False)
     assert layer.sync_status()[0] == 0
+
+
+@pytest.mark.parametrize("T", [600, 2300])
+def test_fused_epilogue_beside_other_work(tiny, T):
+    """The fused epilogue takes its tiles from a work counter, so its value
+    tiles' waits never depend on a CTA that has not started: run while bf16
+    matmuls on another stream hold SMs (600 and 2,300 tokens, both on CTA
+    pairs), it still finishes with status 0 and equals lookup_project +
+    gate_apply bit for bit."""
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    dev = tiny["dev"]
+    fused = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=2300,
+                        fuse_gate=True)
+    try:
+        w, inp = _inputs(tiny, 1, T, mask_frac=0.1, seed=23)
+        ids, x, mask = _dev(inp)
+        ref = fused.gate_apply(fused.lookup_project(ids), x, mask)
+        a = torch.randn(8192, 8192, dtype=torch.bfloat16, device="cuda")
+        b = torch.randn(8192, 8192, dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            for _ in range(8):
+                torch.mm(a, b)
+        outs = [fused.forward(ids, x, mask) for _ in range(4)]
+        torch.cuda.synchronize()
+        assert fused.sync_status()[0] == 0
+        for out in outs:
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    finally:
+        fused.close()
