@@ -499,3 +499,40 @@ def test_fused_epilogue_beside_other_work(tiny, T):
             assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     finally:
         fused.close()
+
+
+def test_plan_invariants_over_batch_sizes(tiny):
+    """The projection's plan over 1 to 20,000 tokens (queries only, nothing
+    runs): CTA pairs exactly from 256 tokens, the gate in the epilogue
+    exactly from 1,024 (on pairs, whole tiles), split-K only up to 128 tokens,
+    a remainder split only for a last wave of at most a quarter of the grid,
+    an even CTA count on pairs, and forward's kernel count to match; under an
+    SM budget, neither pairs nor the fused epilogue."""
+    from engram_hashed_gram_gb300.layer import EngramLayer
+    dev = tiny["dev"]
+    layer = EngramLayer(tiny["table"], tiny["scale"], dev["wkv"], dev["q"], dev["k"], max_tokens=20000)
+    try:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        for budget in (0, 120):
+            layer.set_sm_budget(budget)
+            cap = sms if budget == 0 else budget
+            for M in list(range(1, 300, 7)) + list(range(300, 20001, 173)) + [128, 129, 255, 256, 1023, 1024]:
+                p = layer.describe_plan(M)
+                k = layer.forward_kernels(M)
+                pairs = budget == 0 and M >= 256
+                fused = budget == 0 and M >= 1024
+                assert p["cta_pairs"] == int(pairs), (M, budget, p)
+                assert p["fused_gate"] == int(fused), (M, budget, p)
+                assert p["splits"] == 1 or M <= 128, (M, p)
+                assert p["ctas"] <= cap, (M, p)
+                if pairs:
+                    assert p["ctas"] % 2 == 0, (M, p)
+                if fused:
+                    assert p["rem_tiles"] == 0 and p["splits"] == 1 and k == 2, (M, p, k)
+                else:
+                    assert k == 3 + (1 if p["rem_tiles"] else 0), (M, p, k)
+                if p["rem_tiles"]:
+                    slots = p["ctas"] // 2 if pairs else p["ctas"]
+                    assert 0 < p["rem_tiles"] <= slots // 4 and 2 <= p["rem_splits"] <= 4, (M, p)
+    finally:
+        layer.close()
